@@ -1,0 +1,26 @@
+"""GB300-native (sm_103a) DSA sparse-attention hot path.
+
+DSA indexer scores -> per-query top-k -> sparse absorbed-MLA attention, as
+hand-written CUDA kernels behind the C ABI in include/dsa.h
+(libdsa_gb300.so).  The Python names below are the same calls, marshalling
+torch CUDA tensors into device pointers and the current stream.
+
+    from deepseek_sparse_attention_indexer_gb300 import indexer_scores, topk, \
+        mla_sparse_attn_prefill, mla_sparse_attn_decode
+"""
+
+_API = ("indexer_scores", "topk", "mla_sparse_attn_prefill", "mla_sparse_attn_decode",
+        "attn_workspace_size", "device_status", "status_string", "load", "lib_path", "DsaError")
+
+__all__ = list(_API) + ["workloads", "build"]
+
+
+def __getattr__(name):
+    # torch is imported only when a library call is first used
+    if name in _API:
+        from . import _lib
+        return getattr(_lib, name)
+    if name == "build":
+        from ._build import build
+        return build
+    raise AttributeError(name)

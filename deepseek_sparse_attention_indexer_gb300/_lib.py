@@ -1,0 +1,183 @@
+"""ctypes binding of libdsa_gb300.so (the C ABI in include/dsa.h).
+
+Argument marshalling only: every step of the path runs in the library's CUDA
+kernels.  Tensors are torch CUDA tensors (PyTorch provides device memory and
+streams); bf16 tensors may be torch.bfloat16 or 16-bit integer views of the
+same bits.  If the library is missing or the device is not sm_103, calls raise
+instead of falling back to anything else.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+from typing import Optional
+
+import torch
+
+from . import _build
+
+DSA_OK = 0
+STATUS_NAMES = {
+    0: "DSA_OK", 1: "DSA_ERR_INVALID_ARG", 2: "DSA_ERR_UNSUPPORTED_SHAPE", 3: "DSA_ERR_MISALIGNED",
+    4: "DSA_ERR_WORKSPACE_TOO_SMALL", 5: "DSA_ERR_CUDA", 6: "DSA_ERR_DEVICE_TIMEOUT",
+    7: "DSA_ERR_DEVICE_BOUNDS", 8: "DSA_ERR_UNSUPPORTED_DEVICE",
+}
+
+# every symbol include/dsa.h declares, with (restype, argtypes)
+_P = ctypes.c_void_p
+_I = ctypes.c_int
+_I64 = ctypes.c_int64
+_SZ = ctypes.c_size_t
+_F = ctypes.c_float
+SIGNATURES = {
+    "dsa_status_string": (ctypes.c_char_p, [ctypes.c_int32]),
+    "dsa_abi_version": (ctypes.c_int, []),
+    "dsa_indexer_scores": (ctypes.c_int32, [_P, _P, _P, _P, _P, _I, _I, _I, _P, _I64, _P]),
+    "dsa_topk_workspace_size": (_SZ, [_I, _I, _I, _I]),
+    "dsa_topk": (ctypes.c_int32, [_P, _I64, _P, _P, _I, _I, _I, _I, _P, _P, _SZ, _P]),
+    "mla_sparse_attn_prefill": (ctypes.c_int32, [_P, _P, _P, _I, _I, _I, _F, _P, _P, _P, _SZ, _P]),
+    "mla_sparse_attn_workspace_size": (_SZ, [_I, _I, _I, _I]),
+    "mla_sparse_attn_decode": (ctypes.c_int32, [_P, _P, _P, _P, _I, _I, _I, _F, _P, _P, _P, _SZ, _P]),
+    "dsa_device_status": (ctypes.c_int32, [_P, ctypes.POINTER(ctypes.c_int32), _I]),
+}
+
+_lock = threading.Lock()
+_lib: Optional[ctypes.CDLL] = None
+
+
+class DsaError(RuntimeError):
+    def __init__(self, fn: str, code: int):
+        self.code = code
+        super().__init__(f"{fn} failed: {STATUS_NAMES.get(code, code)} ({status_string(code)})")
+
+
+def lib_path() -> str:
+    return _build.LIB_PATH
+
+
+def load(path: Optional[str] = None) -> ctypes.CDLL:
+    """Load the library (it must have been built: see __graft_entry__.build())."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            p = path or _build.LIB_PATH
+            if not os.path.exists(p):
+                raise RuntimeError(f"{p} is missing: build the CUDA library first "
+                                   "(python -c 'import __graft_entry__ as g; g.build()')")
+            lib = ctypes.CDLL(p)
+            for name, (res, args) in SIGNATURES.items():
+                f = getattr(lib, name)
+                f.restype = res
+                f.argtypes = args
+            _lib = lib
+    return _lib
+
+
+def status_string(code: int) -> str:
+    return load().dsa_status_string(code).decode()
+
+
+def _check(fn: str, code: int):
+    if code != DSA_OK:
+        raise DsaError(fn, code)
+
+
+def _stream(stream=None) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return int(stream.cuda_stream) if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _ptr(t: Optional[torch.Tensor]) -> Optional[int]:
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("expected a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError("expected a contiguous tensor")
+    return t.data_ptr()
+
+
+def _is16(t: torch.Tensor) -> bool:
+    return t.dtype in (torch.bfloat16, torch.int16, torch.uint16)
+
+
+# ----------------------------------------------------------------------------- entry points
+
+def indexer_scores(q_idx: torch.Tensor, k_idx: torch.Tensor, w: torch.Tensor, q_pos0: torch.Tensor,
+                   kv_len: torch.Tensor, scores: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """scores [B, L, ld] f32 from q_idx [B,L,32,128], k_idx [B,Nmax,128] (bf16), w [B,L,32] f32."""
+    B, L, Hi, Di = q_idx.shape
+    Nmax = k_idx.shape[1]
+    assert _is16(q_idx) and _is16(k_idx) and w.dtype == torch.float32
+    if scores is None:
+        ld = (Nmax + 3) // 4 * 4
+        scores = torch.empty((B, L, ld), dtype=torch.float32, device=q_idx.device)
+    ld = scores.shape[-1]
+    rc = load().dsa_indexer_scores(_ptr(q_idx), _ptr(k_idx), _ptr(w), _ptr(q_pos0), _ptr(kv_len),
+                                   B, L, Nmax, _ptr(scores), ld, _stream(stream))
+    _check("dsa_indexer_scores", rc)
+    return scores
+
+
+def topk(scores: torch.Tensor, q_pos0: torch.Tensor, kv_len: torch.Tensor, Nmax: int, top_k: int,
+         idx: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """idx [B, L, top_k] int32 (ascending key order, -1 padded)."""
+    B, L, ld = scores.shape
+    if idx is None:
+        idx = torch.empty((B, L, top_k), dtype=torch.int32, device=scores.device)
+    rc = load().dsa_topk(_ptr(scores), ld, _ptr(q_pos0), _ptr(kv_len), B, L, Nmax, top_k, _ptr(idx),
+                         None, 0, _stream(stream))
+    _check("dsa_topk", rc)
+    return idx
+
+
+def mla_sparse_attn_prefill(q: torch.Tensor, kv: torch.Tensor, idx: torch.Tensor, scale: float,
+                            out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
+                            want_lse: bool = False, stream=None):
+    """out [L, 64, 512] bf16 (and lse [L, 64] f32) for q [L,64,576], kv [N,576], idx [L,top_k]."""
+    L = q.shape[0]
+    N = kv.shape[0]
+    top_k = idx.shape[-1]
+    assert _is16(q) and _is16(kv) and idx.dtype == torch.int32
+    if out is None:
+        out = torch.empty((L, 64, 512), dtype=torch.bfloat16, device=q.device)
+    if lse is None and want_lse:
+        lse = torch.empty((L, 64), dtype=torch.float32, device=q.device)
+    rc = load().mla_sparse_attn_prefill(_ptr(q), _ptr(kv), _ptr(idx), L, N, top_k, float(scale), _ptr(out),
+                                        _ptr(lse), None, 0, _stream(stream))
+    _check("mla_sparse_attn_prefill", rc)
+    return (out, lse) if want_lse else out
+
+
+def attn_workspace_size(B: int, top_k: int, is_decode: bool = True) -> int:
+    return int(load().mla_sparse_attn_workspace_size(B, 1, top_k, 1 if is_decode else 0))
+
+
+def mla_sparse_attn_decode(q: torch.Tensor, kv: torch.Tensor, kv_len: torch.Tensor, idx: torch.Tensor,
+                           scale: float, out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
+                           workspace: Optional[torch.Tensor] = None, want_lse: bool = False, stream=None):
+    """out [B, 64, 512] bf16 for q [B,64,576], kv [B,Nmax,576], kv_len [B], idx [B,top_k]."""
+    B = q.shape[0]
+    Nmax = kv.shape[1]
+    top_k = idx.shape[-1]
+    if out is None:
+        out = torch.empty((B, 64, 512), dtype=torch.bfloat16, device=q.device)
+    if lse is None and want_lse:
+        lse = torch.empty((B, 64), dtype=torch.float32, device=q.device)
+    ws_bytes = attn_workspace_size(B, top_k)
+    if workspace is None:
+        workspace = torch.empty((ws_bytes,), dtype=torch.uint8, device=q.device)
+    rc = load().mla_sparse_attn_decode(_ptr(q), _ptr(kv), _ptr(kv_len), _ptr(idx), B, Nmax, top_k, float(scale),
+                                       _ptr(out), _ptr(lse), _ptr(workspace), workspace.numel(),
+                                       _stream(stream))
+    _check("mla_sparse_attn_decode", rc)
+    return (out, lse) if want_lse else out
+
+
+def device_status(reset: bool = True, stream=None) -> int:
+    code = ctypes.c_int32(0)
+    rc = load().dsa_device_status(_stream(stream), ctypes.byref(code), 1 if reset else 0)
+    _check("dsa_device_status", rc)
+    return code.value

@@ -1,0 +1,42 @@
+// dsa_internal.h -- host-side helpers shared by the library's translation units.
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cstdint>
+
+#include "../../include/dsa.h"
+
+namespace dsa {
+
+// Number of SMs of the current device (cached per device).
+int device_sm_count();
+// DSA_OK when the current device is compute capability 10.3.
+dsa_status_t check_device();
+// Device address of the sticky error word on the current device (nullptr if
+// it cannot be obtained; kernels then skip the report).
+int32_t* device_status_ptr();
+// Raise the dynamic shared-memory limit of `func` on the current device once.
+dsa_status_t ensure_smem_attr(const void* func, int bytes);
+
+// 2D bf16 tensor map: `rows` rows of `cols` elements (row pitch `row_bytes`),
+// box = box_cols x box_rows, 128-byte swizzle, zero fill out of bounds.
+dsa_status_t make_tmap_bf16_2d(CUtensorMap* map, const void* base, uint64_t cols, uint64_t rows,
+                               uint64_t row_bytes, uint32_t box_cols, uint32_t box_rows);
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+inline int ceil_div(int a, int b) { return (a + b - 1) / b; }
+
+// Launch entry points implemented in the kernel files.
+dsa_status_t launch_indexer(const void* q_idx, const void* k_idx, const float* w, const int32_t* q_pos0,
+                            const int32_t* kv_len, int B, int L, int Nmax, float* scores, int64_t ld,
+                            cudaStream_t stream);
+dsa_status_t launch_topk(const float* scores, int64_t ld, const int32_t* q_pos0, const int32_t* kv_len, int B,
+                         int L, int Nmax, int top_k, int32_t* idx, cudaStream_t stream);
+dsa_status_t launch_attn_prefill(const void* q, const void* kv, const int32_t* idx, int L, int N, int top_k,
+                                 float scale, void* out, float* lse, cudaStream_t stream);
+size_t attn_decode_workspace(int B, int top_k);
+dsa_status_t launch_attn_decode(const void* q, const void* kv, const int32_t* kv_len, const int32_t* idx, int B,
+                                int Nmax, int top_k, float scale, void* out, float* lse, void* workspace,
+                                cudaStream_t stream);
+
+}  // namespace dsa

@@ -1,0 +1,333 @@
+// indexer.cu -- DSA indexer scores on the sm_103a tensor cores.
+//
+// What it computes (exo PR #2539, GLM-5.2/5.3 attention, section "Prefill",
+// bullet "Indexer scores in float32, in one kernel"): for every causal
+// (query i, key j), S[i,j] = sum over the 32 indexer heads h of
+// w[i,h] * relu(qI[i,h,:] . kI[j,:]), summed in float32 in one pass, with the
+// causal mask applied (masked keys hold -inf).
+//
+// How (GB300 design):
+//   * One tcgen05 MMA per key tile: M = 128 keys (the A operand, streamed by
+//     TMA through a 4-stage ring), N = 8 queries x 32 heads = 256 (the B
+//     operand, the group's indexer queries, resident while the CTA walks its
+//     key range), K = 128 (head dim).  The accumulator D[key, (q,h)] lands in
+//     TMEM, double-buffered (2 x 256 columns), so the MMA of tile t+1 overlaps
+//     the epilogue of tile t.
+//   * Because the keys sit on the TMEM lanes, the 32-head reduction of one
+//     (query, key) score lives entirely inside one thread: 32 columns of its
+//     lane, relu, times the head weight, summed -- no cross-thread traffic and
+//     no per-head [L, N] tensor ever exists.  Each warp then stores 32
+//     consecutive keys of a score row (128-byte coalesced stores).
+//   * Warp roles: warp 0 issues TMA, warp 1 issues the MMAs (one thread), warps
+//     2..5 run the epilogue, one TMEM lane quadrant each.
+//   * Work items are (batch, 8-query group, key chunk); CTAs are persistent and
+//     walk the items in a zig-zag order so the triangular causal workload of a
+//     first chunk spreads evenly.  Key tiles past the group's last causal key
+//     issue no MMA: the epilogue only writes -inf there.
+//   * Decode (one query per sequence) uses the same kernel with N = 32.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+
+#include "dsa_internal.h"
+#include "dsa_ptx.cuh"
+
+namespace dsa {
+
+namespace {
+
+constexpr int kHi = DSA_INDEXER_HEADS;  // 32
+constexpr int kDi = DSA_INDEXER_DIM;    // 128
+constexpr int kTileKeys = 128;          // MMA M
+constexpr int kThreads = 192;           // 6 warps
+
+struct IndexerParams {
+    const float* w;
+    const int32_t* q_pos0;
+    const int32_t* kv_len;
+    float* scores;
+    int64_t ld;
+    int B, L, Nmax;
+    int G;        // query groups per batch
+    int n_tiles;  // key tiles per batch row = ceil(Nmax / 128)
+    int NC;       // key chunks per group
+    int CH;       // key tiles per chunk
+    int n_items;  // B * G * NC
+    int32_t* status;  // device error word
+};
+
+template <int QG, int STAGES>
+struct Cfg {
+    static constexpr int N = QG * kHi;                      // MMA N
+    static constexpr int A_HALF = kTileKeys * 64 * 2;       // 16 KB: 128 keys x 64 dims
+    static constexpr int A_BYTES = 2 * A_HALF;              // 32 KB
+    static constexpr int B_HALF = N * 64 * 2;               // N rows x 64 dims
+    static constexpr int B_BYTES = 2 * B_HALF;
+    static constexpr int TMEM_COLS = (2 * N < 32) ? 32 : 2 * N;
+    static constexpr int OFF_A = 0;
+    static constexpr int OFF_B = STAGES * A_BYTES;
+    static constexpr int OFF_BAR = OFF_B + B_BYTES;
+    // barriers: a_full[S], a_empty[S], b_full, b_empty, acc_full[2], acc_empty[2]
+    static constexpr int N_BARS = 2 * STAGES + 6;
+    static constexpr int OFF_TMEM = OFF_BAR + N_BARS * 8;
+    static constexpr int OFF_ABORT = OFF_TMEM + 4;
+    static constexpr int SMEM = OFF_ABORT + 4 + 1024;  // + slack for 1024-byte alignment
+    static constexpr uint32_t IDESC = idesc_bf16_f32(kTileKeys, N, false, false);
+};
+
+struct Item {
+    int b, i0, nq, t_begin, t_end, n_comp_end;  // compute tiles are [t_begin, n_comp_end)
+    int pos0, kl;
+};
+
+__device__ __forceinline__ Item decode_item(const IndexerParams& p, int item, int QG) {
+    Item it;
+    int c = item % p.NC;
+    int bg = item / p.NC;
+    int g = bg % p.G;
+    it.b = bg / p.G;
+    it.i0 = g * QG;
+    it.nq = min(QG, p.L - it.i0);
+    it.t_begin = c * p.CH;
+    it.t_end = min(it.t_begin + p.CH, p.n_tiles);
+    it.pos0 = __ldg(p.q_pos0 + it.b);
+    it.kl = min(__ldg(p.kv_len + it.b), p.Nmax);
+    long long lim_last = min((long long)it.pos0 + it.i0 + it.nq - 1, (long long)it.kl - 1);
+    long long nk = lim_last < 0 ? 0 : lim_last + 1;  // keys [0, nk) have a causal query
+    int comp_tiles = (int)((nk + kTileKeys - 1) / kTileKeys);
+    it.n_comp_end = max(it.t_begin, min(it.t_end, comp_tiles));
+    return it;
+}
+
+// The s-th item of this CTA (zig-zag over waves of gridDim.x items); -1 when done.
+__device__ __forceinline__ int nth_item(const IndexerParams& p, int s) {
+    int base = s * (int)gridDim.x;
+    if (base >= p.n_items) return -1;
+    int k = (s & 1) ? ((int)gridDim.x - 1 - (int)blockIdx.x) : (int)blockIdx.x;
+    int item = base + k;
+    return item < p.n_items ? item : -2;  // -2: no item in this wave for this CTA
+}
+
+template <int QG, int STAGES>
+__global__ void __launch_bounds__(kThreads, 1)
+    indexer_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
+                   const IndexerParams p) {
+    using C = Cfg<QG, STAGES>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t* sA = smem + C::OFF_A;
+    uint8_t* sB = smem + C::OFF_B;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
+    uint64_t* a_full = bars;
+    uint64_t* a_empty = bars + STAGES;
+    uint64_t* b_full = bars + 2 * STAGES;
+    uint64_t* b_empty = b_full + 1;
+    uint64_t* acc_full = b_full + 2;
+    uint64_t* acc_empty = b_full + 4;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_TMEM);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_ABORT);
+
+    const int warp = threadIdx.x / 32;
+    const uint32_t lane = lane_id();
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(&a_full[s], 1);
+            mbar_init(&a_empty[s], 1);
+        }
+        mbar_init(b_full, 1);
+        mbar_init(b_empty, 1);
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(&acc_full[a], 1);
+            mbar_init(&acc_empty[a], 128);
+        }
+        *abort_flag = 0;
+        fence_mbar_init();
+        tma_prefetch_desc(&tmap_q);
+        tma_prefetch_desc(&tmap_k);
+    }
+    if (warp == 1) {
+        tmem_alloc(tmem_slot, C::TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ TMA producer
+        if (lane == 0) {
+            int it = 0, bi = 0;
+            bool ok = true;
+            for (int s = 0; ok; ++s) {
+                int item = nth_item(p, s);
+                if (item == -1) break;
+                if (item < 0) continue;
+                Item I = decode_item(p, item, QG);
+                if (I.n_comp_end <= I.t_begin) continue;
+                if (!(ok = mbar_wait(b_empty, (bi & 1) ^ 1, abort_flag, p.status))) break;
+                ++bi;
+                mbar_arrive_expect_tx(b_full, C::B_BYTES);
+                const int qrow = (I.b * p.L + I.i0) * kHi;
+                tma_load_2d(sB, &tmap_q, b_full, 0, qrow);
+                tma_load_2d(sB + C::B_HALF, &tmap_q, b_full, 64, qrow);
+                for (int t = I.t_begin; t < I.n_comp_end; ++t, ++it) {
+                    const int st = it % STAGES;
+                    if (!(ok = mbar_wait(&a_empty[st], ((it / STAGES) & 1) ^ 1, abort_flag, p.status))) break;
+                    mbar_arrive_expect_tx(&a_full[st], C::A_BYTES);
+                    const int krow = I.b * p.Nmax + t * kTileKeys;
+                    uint8_t* dst = sA + st * C::A_BYTES;
+                    tma_load_2d(dst, &tmap_k, &a_full[st], 0, krow);
+                    tma_load_2d(dst + C::A_HALF, &tmap_k, &a_full[st], 64, krow);
+                }
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            int it = 0, bi = 0, acc_it = 0;
+            bool ok = true;
+            for (int s = 0; ok; ++s) {
+                int item = nth_item(p, s);
+                if (item == -1) break;
+                if (item < 0) continue;
+                Item I = decode_item(p, item, QG);
+                if (I.n_comp_end <= I.t_begin) continue;
+                if (!(ok = mbar_wait(b_full, bi & 1, abort_flag, p.status))) break;
+                ++bi;
+                tc_fence_after();
+                const uint32_t b_base = smem_u32(sB);
+                for (int t = I.t_begin; t < I.n_comp_end; ++t, ++it, ++acc_it) {
+                    const int st = it % STAGES;
+                    const int acc = acc_it & 1;
+                    if (!(ok = mbar_wait(&a_full[st], (it / STAGES) & 1, abort_flag, p.status))) break;
+                    if (!(ok = mbar_wait(&acc_empty[acc], ((acc_it >> 1) & 1) ^ 1, abort_flag, p.status))) break;
+                    tc_fence_after();
+                    const uint32_t a_base = smem_u32(sA + st * C::A_BYTES);
+                    const uint32_t d = tmem_base + acc * C::N;
+#pragma unroll
+                    for (int kb = 0; kb < 2; ++kb) {
+#pragma unroll
+                        for (int kk = 0; kk < 4; ++kk) {
+                            uint64_t ad = sdesc_sw128(a_base + kb * C::A_HALF + kk * 32, 16, 1024);
+                            uint64_t bd = sdesc_sw128(b_base + kb * C::B_HALF + kk * 32, 16, 1024);
+                            mma_bf16_ss(d, ad, bd, C::IDESC, (kb | kk) != 0);
+                        }
+                    }
+                    mma_commit(&a_empty[st]);
+                    mma_commit(&acc_full[acc]);
+                }
+                if (ok) mma_commit(b_empty);
+            }
+        }
+    } else {
+        // ------------------------------------------------------------ epilogue (warps 2..5)
+        const int quad = warp & 3;                   // TMEM lane quadrant of this warp
+        const int key_in_tile = quad * 32 + (int)lane;
+        const uint32_t lane_addr = static_cast<uint32_t>(quad * 32) << 16;
+        int acc_it = 0;
+        bool ok = true;
+        for (int s = 0; ok; ++s) {
+            int item = nth_item(p, s);
+            if (item == -1) break;
+            if (item < 0) continue;
+            Item I = decode_item(p, item, QG);
+            const int64_t row0 = (int64_t)I.b * p.L + I.i0;
+            for (int t = I.t_begin; t < I.t_end; ++t) {
+                const int j = t * kTileKeys + key_in_tile;
+                float* srow = p.scores + row0 * p.ld + j;
+                if (t < I.n_comp_end) {
+                    const int acc = acc_it & 1;
+                    if (!(ok = mbar_wait(&acc_full[acc], (acc_it >> 1) & 1, abort_flag, p.status))) break;
+                    tc_fence_after();
+                    const float4* w4 = reinterpret_cast<const float4*>(p.w + row0 * kHi);
+#pragma unroll 1
+                    for (int q = 0; q < QG; ++q) {
+                        uint32_t v[32];
+                        tmem_ld32(tmem_base + lane_addr + acc * C::N + q * kHi, v);
+                        tmem_ld_wait();
+                        float sacc = 0.f;
+                        if (q < I.nq) {
+#pragma unroll
+                            for (int h4 = 0; h4 < kHi / 4; ++h4) {
+                                const float4 wv = __ldg(w4 + q * (kHi / 4) + h4);
+                                sacc = fmaf(wv.x, fmaxf(__uint_as_float(v[4 * h4 + 0]), 0.f), sacc);
+                                sacc = fmaf(wv.y, fmaxf(__uint_as_float(v[4 * h4 + 1]), 0.f), sacc);
+                                sacc = fmaf(wv.z, fmaxf(__uint_as_float(v[4 * h4 + 2]), 0.f), sacc);
+                                sacc = fmaf(wv.w, fmaxf(__uint_as_float(v[4 * h4 + 3]), 0.f), sacc);
+                            }
+                            const long long lim = min((long long)I.pos0 + I.i0 + q, (long long)I.kl - 1);
+                            if (j < p.Nmax) srow[(int64_t)q * p.ld] = ((long long)j <= lim) ? sacc : -INFINITY;
+                        }
+                    }
+                    tc_fence_before();
+                    mbar_arrive(&acc_empty[acc]);
+                    ++acc_it;
+                } else if (j < p.Nmax) {
+                    for (int q = 0; q < I.nq; ++q) srow[(int64_t)q * p.ld] = -INFINITY;
+                }
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, C::TMEM_COLS);
+    }
+}
+
+template <int QG, int STAGES>
+dsa_status_t launch_impl(const void* q_idx, const void* k_idx, const IndexerParams& prm, int B, int L, int Nmax,
+                         cudaStream_t stream) {
+    using C = Cfg<QG, STAGES>;
+    CUtensorMap tq, tk;
+    dsa_status_t st;
+    if ((st = make_tmap_bf16_2d(&tq, q_idx, kDi, (uint64_t)B * L * kHi, kDi * 2, 64, QG * kHi)) != DSA_OK) return st;
+    if ((st = make_tmap_bf16_2d(&tk, k_idx, kDi, (uint64_t)B * Nmax, kDi * 2, 64, kTileKeys)) != DSA_OK) return st;
+    auto kern = indexer_kernel<QG, STAGES>;
+    if ((st = ensure_smem_attr(reinterpret_cast<const void*>(kern), C::SMEM)) != DSA_OK) return st;
+    int grid = min(prm.n_items, device_sm_count());
+    kern<<<grid, kThreads, C::SMEM, stream>>>(tq, tk, prm);
+    return cudaGetLastError() == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
+}
+
+}  // namespace
+
+dsa_status_t launch_indexer(const void* q_idx, const void* k_idx, const float* w, const int32_t* q_pos0,
+                            const int32_t* kv_len, int B, int L, int Nmax, float* scores, int64_t ld,
+                            cudaStream_t stream) {
+    const int QG = (L == 1) ? 1 : 8;
+    IndexerParams p;
+    p.w = w;
+    p.q_pos0 = q_pos0;
+    p.kv_len = kv_len;
+    p.scores = scores;
+    p.ld = ld;
+    p.B = B;
+    p.L = L;
+    p.Nmax = Nmax;
+    p.G = ceil_div(L, QG);
+    p.n_tiles = ceil_div(Nmax, kTileKeys);
+    const int sms = device_sm_count();
+    // Enough items for a few per CTA (load balance), long chunks otherwise
+    // (the group's queries are loaded once per item).
+    const long long groups = (long long)B * p.G;
+    long long nc = (4LL * sms + groups - 1) / groups;
+    if (nc < 1) nc = 1;
+    if (nc > p.n_tiles) nc = p.n_tiles;
+    p.CH = ceil_div(p.n_tiles, (int)nc);
+    p.NC = ceil_div(p.n_tiles, p.CH);
+    long long items = groups * p.NC;
+    if (items > 0x7FFFFFFFLL) return DSA_ERR_UNSUPPORTED_SHAPE;
+    p.n_items = (int)items;
+    p.status = device_status_ptr();
+    if (QG == 8) return launch_impl<8, 4>(q_idx, k_idx, p, B, L, Nmax, stream);
+    return launch_impl<1, 4>(q_idx, k_idx, p, B, L, Nmax, stream);
+}
+
+}  // namespace dsa

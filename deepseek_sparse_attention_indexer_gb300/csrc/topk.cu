@@ -1,0 +1,214 @@
+// topk.cu -- per-query top-k key selection over float32 indexer scores.
+//
+// What it computes (exo PR #2539, section "Prefill": each query keeps its
+// index_topk = 2048 best keys; bullet "The first 2048 queries attend causally":
+// a query with n <= top_k causal keys keeps all of them).  Readings of what the
+// pages leave open: equal scores rank the lower key index first, -0.0 equals
+// +0.0, the selection is written in ascending key order and unused slots hold -1.
+//
+// How: one CTA per score row runs an exact radix select in shared memory.
+//   * Scores map to order-preserving 32-bit keys (-0.0 folded onto +0.0).
+//   * Up to three histogram passes (12 + 12 + 8 bits, shared-memory atomics)
+//     narrow down the threshold key T and how many keys equal to T are still
+//     needed; a pass is skipped as soon as the threshold bucket is taken whole.
+//   * A final pass walks the row in index order and compacts the chosen keys
+//     with block-wide prefix sums: every key above T, plus the first `need`
+//     keys equal to T (this is the lower-index tie rule).  Positions come from
+//     the prefix sums, so the output is ascending without a sort.
+//   * The first pass reads the row from HBM; later passes hit L2.
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "dsa_internal.h"
+
+namespace dsa {
+
+namespace {
+
+constexpr int kThreads = 512;
+constexpr int kWarps = kThreads / 32;
+constexpr int kBins = 4096;
+
+struct TopkParams {
+    const float* scores;
+    int64_t ld;
+    const int32_t* q_pos0;
+    const int32_t* kv_len;
+    int32_t* idx;
+    int B, L, Nmax, K;
+};
+
+__device__ __forceinline__ uint32_t order_key(float f) {
+    uint32_t u = __float_as_uint(f);
+    if (u == 0x80000000u) u = 0u;  // -0.0 == +0.0
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+// Block-wide exclusive scan of one uint32 per thread; returns the exclusive
+// prefix and writes the block total to *total.  Uses warp_sums[kWarps + 1].
+__device__ __forceinline__ uint32_t block_excl_scan(uint32_t v, uint32_t* warp_sums, uint32_t* total) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    uint32_t x = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        uint32_t y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+    }
+    if (lane == 31) warp_sums[warp] = x;
+    __syncthreads();
+    if (warp == 0) {
+        uint32_t s = lane < kWarps ? warp_sums[lane] : 0u;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            uint32_t y = __shfl_up_sync(0xffffffffu, s, o);
+            if (lane >= o) s += y;
+        }
+        if (lane < kWarps) warp_sums[lane] = s;  // inclusive over warps
+        if (lane == kWarps - 1) warp_sums[kWarps] = s;
+    }
+    __syncthreads();
+    uint32_t excl = x - v + (warp > 0 ? warp_sums[warp - 1] : 0u);
+    *total = warp_sums[kWarps];
+    __syncthreads();
+    return excl;
+}
+
+// Given hist[nbins] of the still-tied keys and `need` (>= 1, <= their count),
+// find the bin B* (scanning from the largest bin down) holding the need-th
+// largest key.  Writes sel[0] = B*, sel[1] = need minus the keys in bins above.
+__device__ void find_bin(const uint32_t* hist, int nbins, uint32_t need, uint32_t* warp_sums, uint32_t* sel) {
+    const int per = nbins / kThreads;  // 8 for 4096 bins, 1 for 256 bins (others idle)
+    uint32_t local = 0;
+    const int t = threadIdx.x;
+    const bool active = (per > 0) ? true : (t < nbins);
+    const int p = per > 0 ? per : 1;
+    // thread t owns bins (from the top) [t*p, t*p + p)
+    if (active)
+        for (int k = 0; k < p; ++k) local += hist[nbins - 1 - (t * p + k)];
+    uint32_t total;
+    uint32_t above = block_excl_scan(local, warp_sums, &total);
+    if (active && above < need && above + local >= need) {
+        uint32_t run = above;
+        for (int k = 0; k < p; ++k) {
+            int bin = nbins - 1 - (t * p + k);
+            uint32_t c = hist[bin];
+            if (run + c >= need) {
+                sel[0] = (uint32_t)bin;
+                sel[1] = need - run;
+                sel[2] = c;  // keys in the threshold bin
+                break;
+            }
+            run += c;
+        }
+    }
+    __syncthreads();
+}
+
+__global__ void __launch_bounds__(kThreads) topk_kernel(const TopkParams p) {
+    __shared__ uint32_t hist[kBins];
+    __shared__ uint32_t warp_sums[kWarps + 1];
+    __shared__ uint32_t sel[3];
+
+    const int R = p.B * p.L;
+    for (int r = blockIdx.x; r < R; r += gridDim.x) {
+        const int b = r / p.L, i = r % p.L;
+        const long long pos = (long long)__ldg(p.q_pos0 + b) + i;
+        const long long kl = min((long long)__ldg(p.kv_len + b), (long long)p.Nmax);
+        long long n_ll = min(pos + 1, kl);
+        const int n = (int)max(0LL, n_ll);
+        int32_t* out = p.idx + (int64_t)r * p.K;
+        if (n <= p.K) {
+            for (int t = threadIdx.x; t < p.K; t += kThreads) out[t] = t < n ? t : -1;
+            continue;
+        }
+        const float* row = p.scores + (int64_t)r * p.ld;
+        const float4* row4 = reinterpret_cast<const float4*>(row);
+        const int n4 = (n + 3) / 4;
+
+        // ---- radix narrowing: (shift, prefix, need) describe the threshold class
+        int shift = 32;        // keys compared on bits [shift, 32); 32 = nothing fixed yet
+        uint32_t prefix = 0;
+        uint32_t need = (uint32_t)p.K;
+        const int digit_bits[3] = {12, 12, 8};
+        for (int pass = 0; pass < 3; ++pass) {
+            const int bits = digit_bits[pass];
+            const int nbins = 1 << bits;
+            const int new_shift = shift - bits;
+            for (int k = threadIdx.x; k < nbins; k += kThreads) hist[k] = 0u;
+            __syncthreads();
+            for (int v = threadIdx.x; v < n4; v += kThreads) {
+                const float4 f = __ldcg(row4 + v);
+                const float e[4] = {f.x, f.y, f.z, f.w};
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    if (4 * v + k < n) {
+                        const uint32_t key = order_key(e[k]);
+                        const bool in_class = (shift == 32) || ((key >> shift) == prefix);
+                        if (in_class) atomicAdd(&hist[(key >> new_shift) & (uint32_t)(nbins - 1)], 1u);
+                    }
+                }
+            }
+            __syncthreads();
+            find_bin(hist, nbins, need, warp_sums, sel);
+            const uint32_t bin = sel[0], rem = sel[1], cnt = sel[2];
+            prefix = (shift == 32 ? 0u : (prefix << bits)) | bin;
+            shift = new_shift;
+            need = rem;
+            __syncthreads();
+            if (rem == cnt) break;  // the whole threshold bucket is taken
+        }
+
+        // ---- ordered compaction: keys above the class, then the first `need` of the class
+        uint32_t g_base = 0, e_base = 0;
+        for (int base4 = 0; base4 < n4; base4 += kThreads) {
+            const int v = base4 + threadIdx.x;
+            uint32_t gmask = 0, emask = 0;
+            if (v < n4) {
+                const float4 f = __ldcg(row4 + v);
+                const float e[4] = {f.x, f.y, f.z, f.w};
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    if (4 * v + k < n) {
+                        const uint32_t key = order_key(e[k]) >> shift;
+                        if (key > prefix) gmask |= 1u << k;
+                        else if (key == prefix) emask |= 1u << k;
+                    }
+                }
+            }
+            const uint32_t packed = ((uint32_t)__popc(emask) << 16) | (uint32_t)__popc(gmask);
+            uint32_t total;
+            const uint32_t pre = block_excl_scan(packed, warp_sums, &total);
+            uint32_t g_before = g_base + (pre & 0xFFFFu);
+            uint32_t e_before = e_base + (pre >> 16);
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const int j = 4 * v + k;
+                if (gmask & (1u << k)) {
+                    const uint32_t pos = g_before + min(need, e_before);
+                    if (pos < (uint32_t)p.K) out[pos] = j;
+                    ++g_before;
+                } else if (emask & (1u << k)) {
+                    if (e_before < need && g_before + e_before < (uint32_t)p.K) out[g_before + e_before] = j;
+                    ++e_before;
+                }
+            }
+            g_base += total & 0xFFFFu;
+            e_base += total >> 16;
+        }
+        __syncthreads();
+    }
+}
+
+}  // namespace
+
+dsa_status_t launch_topk(const float* scores, int64_t ld, const int32_t* q_pos0, const int32_t* kv_len, int B,
+                         int L, int Nmax, int top_k, int32_t* idx, cudaStream_t stream) {
+    TopkParams p{scores, ld, q_pos0, kv_len, idx, B, L, Nmax, top_k};
+    const long long R = (long long)B * L;
+    const int grid = (int)min(R, (long long)device_sm_count() * 4);
+    topk_kernel<<<grid, kThreads, 0, stream>>>(p);
+    return cudaGetLastError() == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
+}
+
+}  // namespace dsa

@@ -1,0 +1,164 @@
+/*
+ * dsa.h -- C ABI of libdsa_gb300.so: the DeepSeek / GLM-5.x sparse-attention
+ * hot path (DSA indexer -> per-query top-k -> sparse absorbed-MLA attention)
+ * as hand-written CUDA kernels for sm_103a (GB300).
+ *
+ * Conventions shared by every entry point
+ *   - All tensor pointers are DEVICE pointers owned by the caller.  The library
+ *     never allocates, frees or reads device memory on the host, and never
+ *     synchronises the stream.  The only global state is a sticky device error
+ *     word (dsa_device_status) and per-kernel launch attributes set once.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).
+ *     Every call is asynchronous and ordered on that stream.
+ *   - bf16 tensors are raw IEEE bfloat16 bit patterns, row-major, contiguous,
+ *     with the base 16-byte aligned.
+ *   - Errors are return codes; nothing is thrown across the ABI and the process
+ *     is never aborted.  Argument errors are found on the host before any
+ *     launch.  Inside kernels, an index outside the cache or a wait that runs
+ *     past its limit is recorded in the device status word and the access is
+ *     skipped (no trap).
+ *   - The model constants are fixed to the GLM-5.x layer traced on the pages
+ *     (SlimServe "GLM52_PIPELINE_TRACE.md", Config line; exo PR #2539,
+ *     section Prefill): 32 indexer heads of width 128, 64 attention heads,
+ *     576-wide absorbed query/key ([512 latent | 64 rope]), 512-wide latent V.
+ *     Other shapes are DSA_ERR_UNSUPPORTED_SHAPE: there is no fallback path.
+ */
+#ifndef DSA_GB300_H
+#define DSA_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define DSA_ABI_VERSION 1
+
+#define DSA_INDEXER_HEADS 32
+#define DSA_INDEXER_DIM 128
+#define DSA_HEADS 64
+#define DSA_QK_DIM 576
+#define DSA_V_DIM 512
+#define DSA_MAX_TOPK 2048
+
+typedef int32_t dsa_status_t;
+
+enum {
+    DSA_OK = 0,
+    DSA_ERR_INVALID_ARG = 1,         /* null pointer, non-positive size, bad stride */
+    DSA_ERR_UNSUPPORTED_SHAPE = 2,   /* head count / width / top_k outside what is built */
+    DSA_ERR_MISALIGNED = 3,          /* base pointer or row stride not 16-byte aligned */
+    DSA_ERR_WORKSPACE_TOO_SMALL = 4, /* ws_bytes below the matching *_workspace_size() */
+    DSA_ERR_CUDA = 5,                /* a CUDA runtime call or launch failed */
+    DSA_ERR_DEVICE_TIMEOUT = 6,      /* (device word) an in-kernel wait hit its limit */
+    DSA_ERR_DEVICE_BOUNDS = 7,       /* (device word) an index outside the cache was met */
+    DSA_ERR_UNSUPPORTED_DEVICE = 8   /* current device is not compute capability 10.3 */
+};
+
+/* Text for a status code (static storage, never NULL). */
+const char *dsa_status_string(dsa_status_t status);
+
+/* DSA_ABI_VERSION of the loaded library. */
+int dsa_abi_version(void);
+
+/*
+ * dsa_indexer_scores -- DSA indexer scores, float32, causal mask applied.
+ * Defined on exo PR #2539 (GLM-5.2/5.3 attention), section "Prefill", bullet
+ * "Indexer scores in float32, in one kernel": a key's score is relu(q_h . k)
+ * times head h's weight, summed over the 32 indexer heads in float32 in one
+ * pass with the mask applied (no per-head [L, N] tensors).
+ *
+ *   scores[b, i, j] = sum_{h<32} w[b,i,h] * relu( sum_{d<128} q_idx[b,i,h,d] * k_idx[b,j,d] )
+ *                     for j <= min(q_pos0[b] + i, kv_len[b] - 1)
+ *   scores[b, i, j] = -inf for the other j < Nmax          (columns >= Nmax untouched)
+ *
+ *   q_idx   bf16 [B, L, 32, 128]   indexer queries (post-RoPE)
+ *   k_idx   bf16 [B, Nmax, 128]    indexer keys (post-RoPE)
+ *   w       f32  [B, L, 32]        per-head weights (any scale folded in)
+ *   q_pos0  int32 [B] (device)     position of query 0 of batch b; query i sits at q_pos0[b]+i
+ *   kv_len  int32 [B] (device)     keys present in batch b's cache (<= Nmax)
+ *   scores  f32  [B, L, ld]        output; ld >= Nmax, ld % 4 == 0
+ * Prefill is B = 1 with L queries; batched decode is L = 1 with B sequences.
+ * Products are exact bf16 x bf16 in the tensor core, accumulated in float32.
+ */
+dsa_status_t dsa_indexer_scores(const void *q_idx, const void *k_idx, const float *w,
+                                const int32_t *q_pos0, const int32_t *kv_len, int B, int L,
+                                int Nmax, float *scores, int64_t ld, void *stream);
+
+/*
+ * dsa_topk -- per-query selection of the top_k best-scored causal keys.
+ * Defined on exo PR #2539, section "Prefill": each query keeps its top_k
+ * (index_topk = 2048) keys; "The first 2048 queries attend causally": a query
+ * whose causal key count n = min(q_pos0[b] + i + 1, kv_len[b]) is <= top_k
+ * selects every key 0..n-1.  Readings of points the pages leave open:
+ * equal scores rank the lower key index first; -0.0 equals +0.0; the chosen
+ * indices are written in ascending order; unused slots hold -1.
+ *
+ *   scores  f32 [B, L, ld] (as written by dsa_indexer_scores; only j < n is read)
+ *   idx     int32 [B, L, top_k] output, ascending, -1 padded
+ *   1 <= top_k <= 2048; ld >= Nmax, ld % 4 == 0.  Scores must be finite or -inf.
+ * Needs no workspace (dsa_topk_workspace_size returns 0; pass NULL, 0).
+ */
+size_t dsa_topk_workspace_size(int B, int L, int Nmax, int top_k);
+dsa_status_t dsa_topk(const float *scores, int64_t ld, const int32_t *q_pos0,
+                      const int32_t *kv_len, int B, int L, int Nmax, int top_k, int32_t *idx,
+                      void *workspace, size_t ws_bytes, void *stream);
+
+/*
+ * mla_sparse_attn_prefill -- absorbed-MLA attention of L queries over their
+ * selected keys of one latent cache.
+ * Defined on SlimServe "GLM52_PIPELINE_TRACE.md", section 6 "Attention core
+ * (absorbed MLA)": Q = [q_nope . wk_b (512) | q_pe (64)], K = [kv_cmpr (512) |
+ * k_pe (64)], V = kv_cmpr; scores K.Q times kq_scale, softmax, then V.softmax.
+ * exo PR #2539, section "Prefill": each query gathers only its selected keys;
+ * scaling, masking and the float32 softmax are fused.
+ *
+ *   out[i, h, :] = sum_t softmax_t(scale * q[i,h,:] . kv[idx[i,t], :]) * kv[idx[i,t], 0:512]
+ * over the entries t with idx[i,t] >= 0 (negative entries are skipped).
+ *   q    bf16 [L, 64, 576]     absorbed queries
+ *   kv   bf16 [N, 576]         latent cache rows [kv_cmpr | k_pe]
+ *   idx  int32 [L, top_k]      selected keys (from dsa_topk); entries >= N are
+ *                              recorded as DSA_ERR_DEVICE_BOUNDS and skipped
+ *   out  bf16 [L, 64, 512]     output (round to nearest even from float32)
+ *   lse  f32 [L, 64] or NULL   natural-log sum of exp of the scaled scores
+ * A row with no selected key writes zeros and lse = -inf.
+ * scale is the softmax scale (1/sqrt(192 + 64) = 1/16 for GLM-5.x).
+ * Needs no workspace for prefill (pass NULL, 0).
+ */
+dsa_status_t mla_sparse_attn_prefill(const void *q, const void *kv, const int32_t *idx, int L,
+                                     int N, int top_k, float scale, void *out, float *lse,
+                                     void *workspace, size_t ws_bytes, void *stream);
+
+/*
+ * mla_sparse_attn_decode -- the same attention for one new token in each of B
+ * independent sequences (exo PR #2539, section "Decode", bullet "Decode
+ * attention as GEMMs": the 64 heads of a token share its selected latent
+ * keys, so scores and values are two products over those keys).  The selected
+ * keys of a sequence are split across CTAs and the partial results merged by a
+ * second kernel, through the caller's workspace.
+ *
+ *   q       bf16 [B, 64, 576]; kv bf16 [B, Nmax, 576]; kv_len int32 [B] (device)
+ *   idx     int32 [B, top_k]   (entries >= kv_len[b] recorded as bounds errors, skipped)
+ *   out     bf16 [B, 64, 512]; lse f32 [B, 64] or NULL
+ *   workspace  device buffer of at least mla_sparse_attn_workspace_size(B, 1, top_k, 1)
+ *              bytes, 16-byte aligned; its contents need no initialisation.
+ */
+size_t mla_sparse_attn_workspace_size(int B, int L, int top_k, int is_decode);
+dsa_status_t mla_sparse_attn_decode(const void *q, const void *kv, const int32_t *kv_len,
+                                    const int32_t *idx, int B, int Nmax, int top_k, float scale,
+                                    void *out, float *lse, void *workspace, size_t ws_bytes,
+                                    void *stream);
+
+/*
+ * dsa_device_status -- synchronise `stream`, then read (and if `reset` is
+ * non-zero, clear) the sticky device error word.  *code_out receives DSA_OK,
+ * DSA_ERR_DEVICE_TIMEOUT or DSA_ERR_DEVICE_BOUNDS (timeout wins if both).
+ */
+dsa_status_t dsa_device_status(void *stream, int32_t *code_out, int reset);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DSA_GB300_H */
