@@ -1,0 +1,378 @@
+#!/usr/bin/env python
+"""Benchmark of the DSA sparse-attention hot path on GB300.
+
+One step = one pass of the whole path over one 4096-query prefill chunk at
+16k keys of context (4096 queries at positions 12288..16383, top_k 2048):
+DSA indexer scores -> top-k selection -> sparse absorbed-MLA attention, the
+three C-ABI calls of libdsa_gb300.so on inputs resident in HBM.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+
+Prints one JSON line (rank 0).  Under torchrun each rank processes its own
+chunk on its own GPU (independent problems, no data-path collective), so
+`value` is the chunk queries of all ranks divided by the slowest rank's time
+(weak scaling).  `--impl reference` times the float64 CPU oracle instead, on
+the host cores, on a bounded sample of the same workload.
+"""
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from deepseek_sparse_attention_indexer_gb300 import workloads as W  # noqa: E402
+
+METRIC = "prefill queries/s (indexer+top-k+sparse MLA) at 16k ctx; % of roofline"
+UNIT = "queries/s"
+DEFAULT_WORKLOAD = "prefill_16k"
+PEAKS_PATH = os.path.join(ROOT, "MEASURED_PEAKS.json")
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def algorithmic(wl):
+    """Per-step algorithmic work of the path (causal pairs / selected slots only)."""
+    pos = wl.p0 + np.arange(wl.L, dtype=np.int64)
+    pairs = int(np.minimum(pos + 1, wl.N).sum()) * wl.B
+    slots = int(np.minimum(pos + 1, wl.top_k).sum()) * wl.B
+    return {
+        "indexer_flop": pairs * 32 * 128 * 2,
+        "topk_bytes": pairs * 4,
+        "attn_flop": slots * 64 * (576 + 512) * 2,
+        "gather_bytes": slots * 1152,
+        "pairs": pairs,
+        "slots": slots,
+    }
+
+
+def load_peaks():
+    try:
+        with open(PEAKS_PATH) as f:
+            return json.load(f), "measured"
+    except (OSError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+# ----------------------------------------------------------------------------- clocks
+
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except OSError:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.thread.join(timeout=2)
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) != 6:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[2:]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------- oracle (CPU) timing
+
+def oracle_sample(wl, inputs, rows, threads):
+    """Run the float64 oracle chain on the given query rows; return seconds."""
+    import oracle
+    qi, ki, w, q, kv, q_pos0, kv_len = inputs
+    t0 = time.perf_counter()
+    S = oracle.indexer(qi, ki, w, q_pos0, kv_len, rows=rows, threads=threads)
+    idx = oracle.topk(S.astype(np.float32), q_pos0, kv_len, wl.B, wl.L, wl.top_k, rows=rows, threads=threads)
+    oracle.attention(q[0], kv, idx, np.zeros(wl.L, np.int32), W.SCALE, rows=rows, threads=threads)
+    return time.perf_counter() - t0
+
+
+def sample_rows(wl, n, seed):
+    rng = np.random.default_rng(seed)
+    return sorted(rng.choice(wl.L, size=min(n, wl.L), replace=False).tolist())
+
+
+def run_reference(args, wl, rank, world):
+    """--impl reference: the oracle as it stands, on this host's cores."""
+    if rank != 0:
+        return 0
+    import oracle
+    oracle.build()
+    inputs = make_inputs(wl)
+    threads = oracle.default_threads()
+    rows_per_step = threads
+    for s in range(args.warmup):
+        oracle_sample(wl, inputs, sample_rows(wl, rows_per_step, 100 + s), threads)
+    tot = 0.0
+    for s in range(args.steps):
+        tot += oracle_sample(wl, inputs, sample_rows(wl, rows_per_step, 1000 + s), threads)
+    value = rows_per_step * args.steps / tot
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * tot / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": config_block(wl, world),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
+                         "sample": f"{rows_per_step} query rows per step (indexer over all causal keys, "
+                                   f"top-k, attention over 2048 keys), {args.steps} steps"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ----------------------------------------------------------------------------- GPU arm
+
+def make_inputs(wl):
+    qi, ki, w = W.make_indexer_inputs(wl)
+    q, kv = W.make_attention_inputs(wl)
+    q_pos0, kv_len = W.positions(wl)
+    return qi, ki, w, q, kv, q_pos0, kv_len
+
+
+def config_block(wl, world):
+    return {"workload": wl.name, "desc": wl.desc, "batch": wl.B, "queries": wl.L, "kv_len": wl.N,
+            "q_pos0": wl.p0, "top_k": wl.top_k, "heads": 64, "qk_dim": 576, "v_dim": 512,
+            "indexer_heads": 32, "indexer_dim": 128, "global_batch": wl.B * wl.L * world,
+            "parallelism": f"replicas{world}" if world > 1 else "single",
+            "l2": "flushed between timed steps (write of a 512 MiB buffer); inputs larger than L2"}
+
+
+def run_gpu(args, wl, rank, world, local_rank):
+    import torch
+    import torch.distributed as dist
+    from deepseek_sparse_attention_indexer_gb300 import _lib as dsa
+
+    torch.cuda.set_device(local_rank)
+    dsa.load()
+    inputs = make_inputs(wl)
+    qi, ki, w, q, kv, q_pos0, kv_len = inputs
+    dev = torch.device("cuda", local_rank)
+
+    def d(a):
+        a = np.ascontiguousarray(a)
+        return torch.from_numpy(a.view(np.int16) if a.dtype == np.uint16 else a).to(dev)
+
+    dqi, dki, dw, dpos, dlen, dq, dkv = map(d, (qi, ki, w, q_pos0, kv_len, q, kv))
+    ld = (wl.N + 3) // 4 * 4
+    S = torch.empty((wl.B, wl.L, ld), dtype=torch.float32, device=dev)
+    idx = torch.empty((wl.B, wl.L, wl.top_k), dtype=torch.int32, device=dev)
+    out = torch.empty((wl.L, 64, 512), dtype=torch.bfloat16, device=dev)
+    flush = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step(ev=None):
+        if ev:
+            ev[0].record(stream)
+        dsa.indexer_scores(dqi, dki, dw, dpos, dlen, scores=S)
+        if ev:
+            ev[1].record(stream)
+        dsa.topk(S, dpos, dlen, wl.N, wl.top_k, idx=idx)
+        if ev:
+            ev[2].record(stream)
+        dsa.mla_sparse_attn_prefill(dq[0], dkv[0], idx[0], W.SCALE, out=out)
+        if ev:
+            ev[3].record(stream)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    if dsa.device_status() != 0:
+        raise RuntimeError("device error word set during warm-up")
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    sampler = ClockSampler(local_rank)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    sampler.start()
+    time.sleep(0.3)
+    for k in range(args.steps):
+        flush.zero_()
+        step(evs[k])
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    clocks = sampler.stop()
+    per = np.array([[evs[k][i].elapsed_time(evs[k][i + 1]) for i in range(3)] for k in range(args.steps)])
+    step_ms = float(per.sum(axis=1).mean())
+    kern_ms = per.mean(axis=0)  # indexer, topk, attention
+    t = torch.tensor([step_ms], dtype=torch.float64, device=dev)
+    if world > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    step_ms_max = float(t.item())
+    status = dsa.device_status()
+
+    # ---- end to end through the public API with host buffers (pinned), copies timed
+    host_in = [torch.from_numpy(np.ascontiguousarray(a.view(np.int16) if a.dtype == np.uint16 else a)).pin_memory()
+               for a in (qi, ki, w, q_pos0, kv_len, q, kv)]
+    host_out = torch.empty((wl.L, 64, 512), dtype=torch.bfloat16).pin_memory()
+    dev_in = [h.to(dev) for h in host_in]
+    h2d = sum(h.numel() * h.element_size() for h in host_in)
+    d2h = host_out.numel() * host_out.element_size()
+
+    def e2e_step():
+        for dv, h in zip(dev_in, host_in):
+            dv.copy_(h, non_blocking=True)
+        a_qi, a_ki, a_w, a_pos, a_len, a_q, a_kv = dev_in
+        dsa.indexer_scores(a_qi, a_ki, a_w, a_pos, a_len, scores=S)
+        dsa.topk(S, a_pos, a_len, wl.N, wl.top_k, idx=idx)
+        dsa.mla_sparse_attn_prefill(a_q[0], a_kv[0], idx[0], W.SCALE, out=out)
+        host_out.copy_(out, non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize()
+    e2e_ms = []
+    for _ in range(max(3, min(args.steps, 10))):
+        flush.zero_()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms.append(e0.elapsed_time(e1))
+    t = torch.tensor([float(np.mean(e2e_ms))], dtype=torch.float64, device=dev)
+    if world > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    e2e_mean = float(t.item())
+
+    if rank != 0:
+        return 0
+
+    work = algorithmic(wl)
+    peaks, peak_kind = load_peaks()
+    peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    attn_tf = work["attn_flop"] / (kern_ms[2] * 1e-3) / 1e12
+    idx_tf = work["indexer_flop"] / (kern_ms[0] * 1e-3) / 1e12
+    topk_gbs = work["topk_bytes"] / (kern_ms[1] * 1e-3) / 1e9
+    traffic = None
+    tpath = os.path.join(ROOT, "profiles", "traffic.json")
+    if os.path.exists(tpath):
+        try:
+            traffic = json.load(open(tpath)).get(wl.name, {}).get("mla_sparse_attn")
+        except ValueError:
+            traffic = None
+    line = {
+        "metric": METRIC,
+        "value": wl.L * wl.B * world / (step_ms_max * 1e-3),
+        "unit": UNIT,
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": max(3, args.warmup),
+        "ms_per_step": step_ms_max,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic",
+        "config": config_block(wl, world),
+        "roofline": {"bound": "tensor", "kernel": "mla_sparse_attn_prefill", "achieved": attn_tf,
+                     "peak": peak, "unit": "TFLOP/s", "frac": attn_tf / peak, "traffic": traffic,
+                     "peak_kind": f"{peak_kind} bf16 dense burst",
+                     "flop_per_launch": work["attn_flop"]},
+        "kernels_ms": {"dsa_indexer_scores": float(kern_ms[0]), "dsa_topk": float(kern_ms[1]),
+                       "mla_sparse_attn_prefill": float(kern_ms[2])},
+        "kernel_rooflines": {
+            "dsa_indexer_scores": {"bound": "tensor", "achieved_tflops": idx_tf, "frac": idx_tf / peak},
+            "dsa_topk": {"bound": "hbm", "achieved_gbs": topk_gbs,
+                         "frac": topk_gbs / float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))},
+            "mla_sparse_attn_prefill": {"bound": "tensor", "achieved_tflops": attn_tf, "frac": attn_tf / peak},
+        },
+        "e2e": {"value": wl.L * wl.B * world / (e2e_mean * 1e-3), "unit": UNIT,
+                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)},
+        "gpu_launches": 3 * args.steps,
+        "clocks": clocks,
+        "device_status": status,
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        import oracle
+        oracle.build()
+        threads = oracle.default_threads()
+        rows = sample_rows(wl, 2 * threads, 7)
+        secs = oracle_sample(wl, inputs, rows, threads)
+        line["cpu_baseline"] = {"value": len(rows) / secs, "unit": UNIT, "cores": threads, "kind": "oracle",
+                                "sample": f"{len(rows)} seeded query rows of the same chunk: indexer over all "
+                                          f"their causal keys, top-k, attention over their 2048 keys"}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(W.WORKLOADS))
+    ap.add_argument("--queries", type=int, default=0,
+                    help="profiling aid: keep the context, time only the last N queries of the chunk")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    wl = W.WORKLOADS[args.workload]
+    if args.queries and args.queries < wl.L:
+        wl = W.custom(f"{wl.name}_last{args.queries}", B=wl.B, L=args.queries, p0=wl.N - args.queries, N=wl.N,
+                      top_k=wl.top_k, seed=wl.seed, rope_std=wl.rope_std, dup_frac=wl.dup_frac)
+    if wl.name.startswith("decode"):
+        raise SystemExit("bench.py times prefill chunks; decode steps are timed by the decode tests")
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        return run_reference(args, wl, rank, world)
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    try:
+        return run_gpu(args, wl, rank, world, local_rank)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -63,29 +63,29 @@ def _ptr(a: np.ndarray) -> int:
 
 
 def _split(rows: Sequence[int], threads: int):
-    rows = list(rows)
-    # contiguous runs of rows -> (begin, end) ranges
+    """Cut the sorted row list into (begin, end, position) runs of consecutive
+    rows; `position` is where row `begin` sits in the compact output."""
     runs = []
-    for r in rows:
+    for k, r in enumerate(rows):
         if runs and runs[-1][1] == r:
             runs[-1][1] = r + 1
         else:
-            runs.append([r, r + 1])
-    # cut long runs so every thread gets work
-    total = len(rows)
-    chunk = max(1, (total + 4 * threads - 1) // (4 * threads))
+            runs.append([r, r + 1, k])
+    chunk = max(1, (len(rows) + 4 * threads - 1) // (4 * threads))
     out = []
-    for b, e in runs:
+    for b, e, k in runs:
         while b < e:
-            out.append((b, min(e, b + chunk)))
-            b += chunk
+            n = min(chunk, e - b)
+            out.append((b, b + n, k))
+            b += n
+            k += n
     return out
 
 
 def _run(fn, ranges, threads: int):
     if threads <= 1 or len(ranges) <= 1:
-        for b, e in ranges:
-            fn(b, e)
+        for be in ranges:
+            fn(*be)
         return
     with ThreadPoolExecutor(max_workers=threads) as ex:
         list(ex.map(lambda be: fn(*be), ranges))
@@ -98,7 +98,7 @@ def default_threads() -> int:
 def indexer(qI: np.ndarray, kI: np.ndarray, w: np.ndarray, q_pos0: np.ndarray,
             kv_len: np.ndarray, rows: Optional[Sequence[int]] = None,
             threads: int = 1) -> np.ndarray:
-    """Scores [B*L, Nmax] float64 (rows not listed stay NaN)."""
+    """Scores float64: [B*L, Nmax], or [len(rows), Nmax] for the sorted `rows`."""
     lib = _load()
     B, L, Hi, Di = qI.shape
     Nmax = kI.shape[1]
@@ -107,29 +107,32 @@ def indexer(qI: np.ndarray, kI: np.ndarray, w: np.ndarray, q_pos0: np.ndarray,
     w = np.ascontiguousarray(w, np.float32)
     q_pos0 = np.ascontiguousarray(q_pos0, np.int32)
     kv_len = np.ascontiguousarray(kv_len, np.int32)
-    S = np.full((B * L, Nmax), np.nan, dtype=np.float64)
-    rows = range(B * L) if rows is None else sorted(rows)
+    rows = list(range(B * L)) if rows is None else sorted(rows)
+    S = np.full((len(rows), Nmax), np.nan, dtype=np.float64)
 
-    def fn(b, e):
+    def fn(b, e, k):
         lib.oracle_indexer(_ptr(qI), _ptr(kI), _ptr(w), _ptr(q_pos0), _ptr(kv_len),
-                           B, L, Nmax, Hi, Di, b, e, _ptr(S))
+                           B, L, Nmax, Hi, Di, b, e, _ptr(S) + k * Nmax * 8)
     _run(fn, _split(rows, threads), threads)
     return S
 
 
 def topk(S: np.ndarray, q_pos0: np.ndarray, kv_len: np.ndarray, B: int, L: int,
          K: int, rows: Optional[Sequence[int]] = None, threads: int = 1) -> np.ndarray:
-    """Top-k indices [B*L, K] int32 from float32 scores [B*L, ld]."""
+    """Top-k indices int32 [B*L, K] from float32 scores [B*L, ld]; with `rows`,
+    the scores and the result hold only those (sorted) rows."""
     lib = _load()
     S = np.ascontiguousarray(S, np.float32)
     q_pos0 = np.ascontiguousarray(q_pos0, np.int32)
     kv_len = np.ascontiguousarray(kv_len, np.int32)
-    idx = np.full((B * L, K), -2, dtype=np.int32)
-    rows = range(B * L) if rows is None else sorted(rows)
+    rows = list(range(B * L)) if rows is None else sorted(rows)
+    assert S.shape[0] == len(rows)
+    idx = np.full((len(rows), K), -2, dtype=np.int32)
+    ld = S.shape[1]
 
-    def fn(b, e):
-        lib.oracle_topk(_ptr(S), S.shape[1], _ptr(q_pos0), _ptr(kv_len), B, L, K,
-                        b, e, _ptr(idx))
+    def fn(b, e, k):
+        lib.oracle_topk(_ptr(S) + k * ld * 4, ld, _ptr(q_pos0), _ptr(kv_len), B, L, K,
+                        b, e, _ptr(idx) + k * K * 4)
     _run(fn, _split(rows, threads), threads)
     return idx
 
@@ -138,7 +141,8 @@ def attention(q: np.ndarray, kv: np.ndarray, idx: np.ndarray, row_batch: np.ndar
               scale: float, rows: Optional[Sequence[int]] = None, threads: int = 1):
     """out [R, H, Dv] float64 and lse [R, H] float64 (Dv = D - 64).
 
-    q [R, H, D] bf16 bits, kv [B, Nmax, D] bf16 bits, idx [R, K] int32.
+    q [R, H, D] bf16 bits, kv [B, Nmax, D] bf16 bits, idx [R, K] int32.  With
+    `rows`, idx, out and lse hold only those (sorted) rows.
     """
     lib = _load()
     R, H, D = q.shape
@@ -150,12 +154,13 @@ def attention(q: np.ndarray, kv: np.ndarray, idx: np.ndarray, row_batch: np.ndar
     kv = np.ascontiguousarray(kv, np.uint16)
     idx = np.ascontiguousarray(idx, np.int32)
     row_batch = np.ascontiguousarray(row_batch, np.int32)
-    out = np.full((R, H, Dv), np.nan, dtype=np.float64)
-    lse = np.full((R, H), np.nan, dtype=np.float64)
-    rows = range(R) if rows is None else sorted(rows)
+    rows = list(range(R)) if rows is None else sorted(rows)
+    assert idx.shape[0] == len(rows)
+    out = np.full((len(rows), H, Dv), np.nan, dtype=np.float64)
+    lse = np.full((len(rows), H), np.nan, dtype=np.float64)
 
-    def fn(b, e):
-        lib.oracle_attn(_ptr(q), _ptr(kv), _ptr(idx), _ptr(row_batch), Nmax, K, H, D, Dv,
-                        float(scale), b, e, _ptr(out), _ptr(lse))
+    def fn(b, e, k):
+        lib.oracle_attn(_ptr(q), _ptr(kv), _ptr(idx) + k * K * 4, _ptr(row_batch), Nmax, K, H, D,
+                        Dv, float(scale), b, e, _ptr(out) + k * H * Dv * 8, _ptr(lse) + k * H * 8)
     _run(fn, _split(rows, threads), threads)
     return out, lse

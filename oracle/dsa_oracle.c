@@ -48,7 +48,8 @@ static double bf16_to_double(uint16_t b)
  * position p_r = q_pos0[b] + i.  Every other key j < Nmax is masked and holds
  * -inf (reading: "with the mask applied" -- a masked key is never selectable).
  * No extra scale is applied: any 1/sqrt constant is taken as folded into w.
- *   qI [B, L, Hi, Di], kI [B, Nmax, Di], w [B, L, Hi], S [B*L, Nmax].
+ *   qI [B, L, Hi, Di], kI [B, Nmax, Di], w [B, L, Hi] (indexed by absolute row);
+ *   S [row_end - row_begin, Nmax]: S[0] is the output of row row_begin.
  */
 void oracle_indexer(const uint16_t *qI, const uint16_t *kI, const float *w,
                     const int32_t *q_pos0, const int32_t *kv_len,
@@ -62,7 +63,7 @@ void oracle_indexer(const uint16_t *qI, const uint16_t *kI, const float *w,
         long last = p < (long)kv_len[b] - 1 ? p : (long)kv_len[b] - 1;
         const uint16_t *q = qI + (size_t)r * Hi * Di;
         const float *wr = w + (size_t)r * Hi;
-        double *srow = S + (size_t)r * Nmax;
+        double *srow = S + (size_t)(r - row_begin) * Nmax;
         for (int j = 0; j < Nmax; ++j) {
             if ((long)j > last) {
                 srow[j] = -INFINITY;
@@ -111,7 +112,8 @@ static int cmp_int_asc(const void *a, const void *b)
  *   n >  K : the K keys j < n with the largest S[r, j]; equal scores are
  *            ordered by the lower key index (tie rule: lower index wins);
  *            -0.0 equals +0.0.  The chosen indices are written ascending.
- * S is [B*L rows, ld]; idx is [B*L, K].
+ * S is [row_end - row_begin, ld] and idx is [row_end - row_begin, K]: their
+ * first row belongs to query row row_begin.
  */
 void oracle_topk(const float *S, int64_t ld, const int32_t *q_pos0, const int32_t *kv_len,
                  int B, int L, int K, int row_begin, int row_end, int32_t *idx)
@@ -122,14 +124,14 @@ void oracle_topk(const float *S, int64_t ld, const int32_t *q_pos0, const int32_
         long p = (long)q_pos0[b] + i;
         long n = p + 1 < (long)kv_len[b] ? p + 1 : (long)kv_len[b];
         if (n < 0) n = 0;
-        int32_t *out = idx + (size_t)r * K;
+        int32_t *out = idx + (size_t)(r - row_begin) * K;
         if (n <= K) {
             for (long t = 0; t < K; ++t) out[t] = t < n ? (int32_t)t : -1;
             continue;
         }
         cand_t *c = (cand_t *)malloc((size_t)n * sizeof *c);
         for (long j = 0; j < n; ++j) {
-            c[j].s = S[(size_t)r * ld + j];
+            c[j].s = S[(size_t)(r - row_begin) * ld + j];
             c[j].j = (int32_t)j;
         }
         qsort(c, (size_t)n, sizeof *c, cmp_score_desc_index_asc);
@@ -149,7 +151,9 @@ void oracle_topk(const float *S, int64_t ld, const int32_t *q_pos0, const int32_
  * There is no softmax bias or sink.  A row that selects nothing gets a zero
  * output and lse = -inf.  row_batch[r] names the batch of each row, so one
  * routine serves prefill rows (all in batch 0) and decode rows (one per batch).
- *   q [R, H, D], kv [B, Nmax, D], idx [R, K], out [R, H, Dv], lse [R, H].
+ *   q [R, H, D] and row_batch [R] are indexed by absolute row; kv [B, Nmax, D];
+ *   idx [row_end - row_begin, K], out [.., H, Dv] and lse [.., H] start at row
+ *   row_begin.
  */
 void oracle_attn(const uint16_t *q, const uint16_t *kv, const int32_t *idx,
                  const int32_t *row_batch, int Nmax, int K, int H, int D, int Dv,
@@ -158,10 +162,10 @@ void oracle_attn(const uint16_t *q, const uint16_t *kv, const int32_t *idx,
     double *s = (double *)malloc((size_t)K * sizeof *s);
     for (int r = row_begin; r < row_end; ++r) {
         int b = row_batch[r];
-        const int32_t *ir = idx + (size_t)r * K;
+        const int32_t *ir = idx + (size_t)(r - row_begin) * K;
         for (int h = 0; h < H; ++h) {
             const uint16_t *qh = q + ((size_t)r * H + h) * D;
-            double *o = out + ((size_t)r * H + h) * Dv;
+            double *o = out + ((size_t)(r - row_begin) * H + h) * Dv;
             for (int v = 0; v < Dv; ++v) o[v] = 0.0;
             int any = 0;
             double m = -INFINITY;
@@ -176,7 +180,7 @@ void oracle_attn(const uint16_t *q, const uint16_t *kv, const int32_t *idx,
                 any = 1;
             }
             if (!any) {
-                lse[(size_t)r * H + h] = -INFINITY;
+                lse[(size_t)(r - row_begin) * H + h] = -INFINITY;
                 continue;
             }
             double sum = 0.0;
@@ -188,7 +192,7 @@ void oracle_attn(const uint16_t *q, const uint16_t *kv, const int32_t *idx,
                 for (int v = 0; v < Dv; ++v) o[v] += e * bf16_to_double(kr[v]);
             }
             for (int v = 0; v < Dv; ++v) o[v] /= sum;
-            lse[(size_t)r * H + h] = m + log(sum);
+            lse[(size_t)(r - row_begin) * H + h] = m + log(sum);
         }
     }
     free(s);
