@@ -10,6 +10,7 @@ torch CUDA tensors into device pointers and the current stream.
 """
 
 _API = ("indexer_scores", "topk", "mla_sparse_attn_prefill", "mla_sparse_attn_decode",
+        "mla_sparse_attn_decode_noalloc",
         "attn_workspace_size", "device_status", "status_string", "load", "lib_path", "DsaError")
 
 __all__ = list(_API) + ["workloads", "build"]

@@ -21,7 +21,7 @@ DSA_OK = 0
 STATUS_NAMES = {
     0: "DSA_OK", 1: "DSA_ERR_INVALID_ARG", 2: "DSA_ERR_UNSUPPORTED_SHAPE", 3: "DSA_ERR_MISALIGNED",
     4: "DSA_ERR_WORKSPACE_TOO_SMALL", 5: "DSA_ERR_CUDA", 6: "DSA_ERR_DEVICE_TIMEOUT",
-    7: "DSA_ERR_DEVICE_BOUNDS", 8: "DSA_ERR_UNSUPPORTED_DEVICE",
+    7: "DSA_ERR_DEVICE_BOUNDS", 8: "DSA_ERR_UNSUPPORTED_DEVICE", 9: "DSA_ERR_SCRATCH_TOO_SMALL",
 }
 
 # every symbol include/dsa.h declares, with (restype, argtypes)
@@ -39,6 +39,7 @@ SIGNATURES = {
     "mla_sparse_attn_prefill": (ctypes.c_int32, [_P, _P, _P, _I, _I, _I, _F, _P, _P, _P, _SZ, _P]),
     "mla_sparse_attn_workspace_size": (_SZ, [_I, _I, _I, _I]),
     "mla_sparse_attn_decode": (ctypes.c_int32, [_P, _P, _P, _P, _I, _I, _I, _F, _P, _P, _P, _SZ, _P]),
+    "mla_sparse_attn_decode_noalloc": (ctypes.c_int32, [_P, _P, _P, _P, _I, _I, _I, _F, _P, _P, _P]),
     "dsa_device_status": (ctypes.c_int32, [_P, ctypes.POINTER(ctypes.c_int32), _I]),
 }
 
@@ -173,6 +174,26 @@ def mla_sparse_attn_decode(q: torch.Tensor, kv: torch.Tensor, kv_len: torch.Tens
                                        _ptr(out), _ptr(lse), _ptr(workspace), workspace.numel(),
                                        _stream(stream))
     _check("mla_sparse_attn_decode", rc)
+    return (out, lse) if want_lse else out
+
+
+def mla_sparse_attn_decode_noalloc(q: torch.Tensor, kv: torch.Tensor, kv_len: torch.Tensor, idx: torch.Tensor,
+                                   scale: float, out: Optional[torch.Tensor] = None,
+                                   lse: Optional[torch.Tensor] = None, want_lse: bool = False, stream=None):
+    """Decode attention without a workspace, for callers that may not allocate
+    device memory: the library keeps the split partials in its own fixed device
+    scratch (B <= 63).  Pass preallocated `out` (and `lse`) to allocate nothing
+    here either.  Calls that overlap on the GPU share that scratch and race."""
+    B = q.shape[0]
+    Nmax = kv.shape[1]
+    top_k = idx.shape[-1]
+    if out is None:
+        out = torch.empty((B, 64, 512), dtype=torch.bfloat16, device=q.device)
+    if lse is None and want_lse:
+        lse = torch.empty((B, 64), dtype=torch.float32, device=q.device)
+    rc = load().mla_sparse_attn_decode_noalloc(_ptr(q), _ptr(kv), _ptr(kv_len), _ptr(idx), B, Nmax, top_k,
+                                               float(scale), _ptr(out), _ptr(lse), _stream(stream))
+    _check("mla_sparse_attn_decode_noalloc", rc)
     return (out, lse) if want_lse else out
 
 

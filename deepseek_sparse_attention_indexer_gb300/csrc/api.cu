@@ -123,6 +123,8 @@ const char* dsa_status_string(dsa_status_t s) {
         case DSA_ERR_DEVICE_TIMEOUT: return "an in-kernel wait ran past its limit";
         case DSA_ERR_DEVICE_BOUNDS: return "a selected key index was outside the cache (access skipped)";
         case DSA_ERR_UNSUPPORTED_DEVICE: return "device is not compute capability 10.3 (sm_103a)";
+        case DSA_ERR_SCRATCH_TOO_SMALL:
+            return "request exceeds the fixed device scratch of mla_sparse_attn_decode_noalloc (B <= 63)";
         default: return "unknown status";
     }
 }
@@ -201,6 +203,21 @@ dsa_status_t mla_sparse_attn_decode(const void* q, const void* kv, const int32_t
     if (st != DSA_OK) return st;
     return launch_attn_decode(q, kv, kv_len, idx, B, Nmax, top_k, scale, out, lse, workspace,
                               static_cast<cudaStream_t>(stream));
+}
+
+dsa_status_t mla_sparse_attn_decode_noalloc(const void* q, const void* kv, const int32_t* kv_len,
+                                            const int32_t* idx, int B, int Nmax, int top_k, float scale, void* out,
+                                            float* lse, void* stream) {
+    if (!q || !kv || !kv_len || !idx || !out) return DSA_ERR_INVALID_ARG;
+    if (B < 1 || Nmax < 1) return DSA_ERR_INVALID_ARG;
+    if (top_k < 1 || top_k > DSA_MAX_TOPK) return DSA_ERR_UNSUPPORTED_SHAPE;
+    if (!(scale > 0.f) || !(scale < 1e30f)) return DSA_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(kv) || !aligned16(out)) return DSA_ERR_MISALIGNED;
+    if (B > DSA_NOALLOC_MAX_BATCH) return DSA_ERR_SCRATCH_TOO_SMALL;
+    dsa_status_t st = check_device();
+    if (st != DSA_OK) return st;
+    return launch_attn_decode_noalloc(q, kv, kv_len, idx, B, Nmax, top_k, scale, out, lse,
+                                      static_cast<cudaStream_t>(stream));
 }
 
 dsa_status_t dsa_device_status(void* stream, int32_t* code_out, int reset) {

@@ -36,6 +36,7 @@
 
 #include <cmath>
 #include <cstdint>
+#include <mutex>
 
 #include "dsa_internal.h"
 #include "dsa_ptx.cuh"
@@ -635,6 +636,71 @@ dsa_status_t launch_attn_decode(const void* q, const void* kv, const int32_t* kv
     p.scale_log2 = scale * 1.4426950408889634f;
     p.status = device_status_ptr();
     dsa_status_t st = launch_kernel<true>(q, B, p, stream);
+    if (st != DSA_OK) return st;
+    mla_decode_combine_kernel<<<B * kH, 128, 0, stream>>>(p.part_o, p.part_lse, p.nsplit,
+                                                         static_cast<__nv_bfloat16*>(out), lse);
+    return cudaGetLastError() == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
+}
+
+// ---------------------------------------------------------------------------
+// Allocation-free decode (mla_sparse_attn_decode_noalloc).  For callers that
+// may not allocate device memory, the split partials live in this fixed
+// file-scope array instead of a caller workspace.  Its name is only a host-side
+// stand-in for the device object, so the host looks up the real device address
+// once per device (cudaGetSymbolAddress, no allocation) and passes it to the
+// kernels.  All calls on a device share it; overlapping calls race.
+namespace {
+constexpr size_t kNoallocScratchBytes = DSA_NOALLOC_SCRATCH_BYTES;
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoallocScratchBytes];
+
+constexpr int kMaxDevicesNoalloc = 64;
+std::mutex g_noalloc_mu;
+void* g_noalloc_ptr[kMaxDevicesNoalloc] = {};
+
+dsa_status_t noalloc_scratch(void** ptr) {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return DSA_ERR_CUDA;
+    if (dev >= kMaxDevicesNoalloc) return DSA_ERR_UNSUPPORTED_DEVICE;
+    std::lock_guard<std::mutex> g(g_noalloc_mu);
+    if (!g_noalloc_ptr[dev]) {
+        void* a = nullptr;
+        if (cudaGetSymbolAddress(&a, g_noalloc_scratch) != cudaSuccess || !a) return DSA_ERR_CUDA;
+        g_noalloc_ptr[dev] = a;
+    }
+    *ptr = g_noalloc_ptr[dev];
+    return DSA_OK;
+}
+}  // namespace
+
+dsa_status_t launch_attn_decode_noalloc(const void* q, const void* kv, const int32_t* kv_len, const int32_t* idx,
+                                        int B, int Nmax, int top_k, float scale, void* out, float* lse,
+                                        cudaStream_t stream) {
+    const size_t per_item = (size_t)kH * (kDv + 1) * sizeof(float);
+    const int max_items = (int)(kNoallocScratchBytes / per_item);
+    if (B > max_items) return DSA_ERR_SCRATCH_TOO_SMALL;
+    void* scratch = nullptr;
+    dsa_status_t st = noalloc_scratch(&scratch);
+    if (st != DSA_OK) return st;
+    const int tiles = ceil_div(top_k, kTile);
+    int ns = decode_splits(B, top_k);
+    if (ns > max_items / B) ns = max_items / B;
+    if (ns < 1) ns = 1;
+    AttnParams p{};
+    p.kv = static_cast<const __nv_bfloat16*>(kv);
+    p.idx = idx;
+    p.kv_len = kv_len;
+    p.part_o = static_cast<float*>(scratch);
+    p.rows = B;
+    p.prefill = 0;
+    p.Nmax = Nmax;
+    p.top_k = top_k;
+    p.split_len = ceil_div(tiles, ns) * kTile;
+    p.nsplit = ceil_div(top_k, p.split_len);
+    p.part_lse = p.part_o + (size_t)B * p.nsplit * kH * kDv;
+    p.n_items = B * p.nsplit;
+    p.scale_log2 = scale * 1.4426950408889634f;
+    p.status = device_status_ptr();
+    st = launch_kernel<true>(q, B, p, stream);
     if (st != DSA_OK) return st;
     mla_decode_combine_kernel<<<B * kH, 128, 0, stream>>>(p.part_o, p.part_lse, p.nsplit,
                                                          static_cast<__nv_bfloat16*>(out), lse);

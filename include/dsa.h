@@ -53,7 +53,8 @@ enum {
     DSA_ERR_CUDA = 5,                /* a CUDA runtime call or launch failed */
     DSA_ERR_DEVICE_TIMEOUT = 6,      /* (device word) an in-kernel wait hit its limit */
     DSA_ERR_DEVICE_BOUNDS = 7,       /* (device word) an index outside the cache was met */
-    DSA_ERR_UNSUPPORTED_DEVICE = 8   /* current device is not compute capability 10.3 */
+    DSA_ERR_UNSUPPORTED_DEVICE = 8,  /* current device is not compute capability 10.3 */
+    DSA_ERR_SCRATCH_TOO_SMALL = 9    /* request does not fit the library's fixed device scratch */
 };
 
 /* Text for a status code (static storage, never NULL). */
@@ -149,6 +150,41 @@ dsa_status_t mla_sparse_attn_decode(const void *q, const void *kv, const int32_t
                                     const int32_t *idx, int B, int Nmax, int top_k, float scale,
                                     void *out, float *lse, void *workspace, size_t ws_bytes,
                                     void *stream);
+
+/*
+ * mla_sparse_attn_decode_noalloc -- mla_sparse_attn_decode for callers that
+ * cannot allocate device memory.  No counterpart in the paper: this is an
+ * integration aid, not part of the method.
+ *
+ * Some callers are not allowed to call cudaMalloc: plugins hosted inside an
+ * engine that owns every byte of device memory through its own pool, or
+ * latency-critical decode loops where a device allocation (which may
+ * synchronise the whole device) is forbidden.  Such callers cannot provide the
+ * split-partials workspace that mla_sparse_attn_decode needs.  This variant
+ * keeps those partials in a fixed scratch array that lives inside the library
+ * (DSA_NOALLOC_SCRATCH_BYTES = 8 MiB on every GPU that loads the library, held
+ * until the process exits).  The caller still passes q, kv, kv_len, idx, out
+ * and lse exactly as for mla_sparse_attn_decode; arguments and results are the
+ * same (the keys of a sequence may be split over fewer CTAs, which changes
+ * only float32 rounding).
+ *
+ *   - B * splits * 64 * 513 * 4 bytes must fit the scratch; this holds for any
+ *     B <= DSA_NOALLOC_MAX_BATCH (63) and top_k <= 2048.  Larger B returns
+ *     DSA_ERR_SCRATCH_TOO_SMALL without launching anything.
+ *   - The first call on a device looks up the scratch's device address (a
+ *     runtime symbol query, no allocation); make that first call before any
+ *     stream capture.
+ *   - Every call on a device shares the one scratch array and it keeps the last
+ *     call's contents (nothing in it needs to start at zero).  Calls whose
+ *     kernels overlap on the GPU (different streams, or different host threads
+ *     without ordering) race on it and give wrong results: serialise them.
+ *   - Allocates nothing: no cudaMalloc / cudaFree and no allocating library call.
+ */
+#define DSA_NOALLOC_SCRATCH_BYTES (8u << 20)
+#define DSA_NOALLOC_MAX_BATCH 63
+dsa_status_t mla_sparse_attn_decode_noalloc(const void *q, const void *kv, const int32_t *kv_len,
+                                            const int32_t *idx, int B, int Nmax, int top_k,
+                                            float scale, void *out, float *lse, void *stream);
 
 /*
  * dsa_device_status -- synchronise `stream`, then read (and if `reset` is

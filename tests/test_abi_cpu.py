@@ -48,7 +48,7 @@ def test_exports_every_declared_symbol(lib):
 
 def test_version_and_strings(lib):
     assert lib.dsa_abi_version() == 1
-    for code in range(0, 9):
+    for code in range(0, 10):
         s = lib.dsa_status_string(code)
         assert s and len(s) > 1
     assert lib.dsa_status_string(12345) == b"unknown status"
