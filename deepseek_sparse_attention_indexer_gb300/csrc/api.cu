@@ -92,8 +92,9 @@ dsa_status_t ensure_smem_attr(const void* func, int bytes) {
     return DSA_OK;
 }
 
-dsa_status_t make_tmap_bf16_2d(CUtensorMap* map, const void* base, uint64_t cols, uint64_t rows, uint64_t row_bytes,
-                               uint32_t box_cols, uint32_t box_rows) {
+namespace {
+dsa_status_t make_tmap_impl(CUtensorMap* map, const void* base, uint64_t cols, uint64_t rows, uint64_t row_bytes,
+                            uint32_t box_cols, uint32_t box_rows, CUtensorMapSwizzle swz) {
     auto fn = encode_fn();
     if (!fn) return DSA_ERR_CUDA;
     cuuint64_t dims[2] = {cols, rows};
@@ -101,9 +102,19 @@ dsa_status_t make_tmap_bf16_2d(CUtensorMap* map, const void* base, uint64_t cols
     cuuint32_t box[2] = {box_cols, box_rows};
     cuuint32_t estr[2] = {1, 1};
     CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
-                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? DSA_OK : DSA_ERR_CUDA;
+}
+}  // namespace
+
+dsa_status_t make_tmap_bf16_2d(CUtensorMap* map, const void* base, uint64_t cols, uint64_t rows, uint64_t row_bytes,
+                               uint32_t box_cols, uint32_t box_rows) {
+    return make_tmap_impl(map, base, cols, rows, row_bytes, box_cols, box_rows, CU_TENSOR_MAP_SWIZZLE_128B);
+}
+dsa_status_t make_tmap_bf16_2d_sw64(CUtensorMap* map, const void* base, uint64_t cols, uint64_t rows,
+                                    uint64_t row_bytes, uint32_t box_cols, uint32_t box_rows) {
+    return make_tmap_impl(map, base, cols, rows, row_bytes, box_cols, box_rows, CU_TENSOR_MAP_SWIZZLE_64B);
 }
 
 }  // namespace dsa

@@ -22,6 +22,9 @@ dsa_status_t ensure_smem_attr(const void* func, int bytes);
 // box = box_cols x box_rows, 128-byte swizzle, zero fill out of bounds.
 dsa_status_t make_tmap_bf16_2d(CUtensorMap* map, const void* base, uint64_t cols, uint64_t rows,
                                uint64_t row_bytes, uint32_t box_cols, uint32_t box_rows);
+// Same with a 64-byte swizzle (box_cols * 2 must be 64).
+dsa_status_t make_tmap_bf16_2d_sw64(CUtensorMap* map, const void* base, uint64_t cols, uint64_t rows,
+                                    uint64_t row_bytes, uint32_t box_cols, uint32_t box_rows);
 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 inline int ceil_div(int a, int b) { return (a + b - 1) / b; }

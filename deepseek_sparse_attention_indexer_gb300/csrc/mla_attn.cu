@@ -21,12 +21,13 @@
 //     chunks + the rope block).  Each segment has its own full/free barrier so
 //     the next tile's chunk c streams in as soon as PV has consumed chunk c.
 //     Unselected or padding slots are zero-filled (never NaN garbage).
-//   * Softmax: 4 warps, one key per thread; per-head maxima are reduced with a
-//     transposing butterfly (62 shuffles per thread for 64 heads) and one
-//     shared-memory exchange.  The running maximum is only raised when a tile
-//     exceeds it by more than 2^8 (rescaling of O^T in TMEM is then rare);
-//     numerator and denominator always use the same maximum, so the result is
-//     the exact softmax.  P^T is written as bf16 into the (consumed) rope block.
+//   * Softmax: 4 warps, one key per thread.  Each head's reference maximum is
+//     taken from the query's first tile (transposing warp butterfly + one
+//     shared-memory exchange); later tiles only check, per thread, whether a
+//     score exceeds its reference by more than 2^16, and only then reduce and
+//     rescale O^T in TMEM.  Numerator and denominator always share the
+//     reference, so the result is the exact softmax.  P^T is written as bf16
+//     into the (consumed) rope block.
 //   * The query's Q^T (72 KB) is loaded by TMA once per query.
 //   * Decode splits a sequence's selected keys over CTAs and writes partial
 //     (normalised output, lse) pairs; a small kernel merges them.
@@ -53,7 +54,7 @@ constexpr int kTile = 128;             // keys per tile (MMA M)
 constexpr int kBlkBytes = kTile * 128; // 16 KB: 128 keys x 64 dims
 constexpr int kQBlkBytes = kH * 128;   // 8 KB: 64 heads x 64 dims
 constexpr int kThreads = 320;          // 10 warps
-constexpr float kRescaleThreshold = 8.0f;  // log2 units
+constexpr float kRescaleThreshold = 16.0f;  // log2 units
 
 // smem layout (1024-aligned base)
 constexpr int OFF_Q = 0;                               // 9 x 8 KB
@@ -398,28 +399,50 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mbar_arrive(s_empty);
                 const int slot = I.slot0 + t * kTile + key;
                 int j = (slot < I.slot_end) ? __ldg(ir + slot) : -1;
-                const bool valid = (j >= 0) && (j < I.bound);
+                if (!((j >= 0) && (j < I.bound))) {
 #pragma unroll
-                for (int h = 0; h < kH; ++h) x[h] = valid ? x[h] * p.scale_log2 : -INFINITY;
-                // tile maxima per head -> shared, then the running-max update for 64 heads
-                float r0, r1;
-                warp_transpose_reduce<true>(x, lane, r0, r1);
-                red[sw * kH + 2 * lane] = r0;
-                red[sw * kH + 2 * lane + 1] = r1;
-                named_bar_sync(1, 128);
-                bool upd = false;
-                if (tid < kH) {
-                    const float mt = fmaxf(fmaxf(red[tid], red[kH + tid]), fmaxf(red[2 * kH + tid], red[3 * kH + tid]));
-                    const float mo = m_used[tid];
-                    float a = 1.f;
-                    if (mt > -INFINITY && (mo == -INFINITY || mt > mo + kRescaleThreshold)) {
-                        a = (mo == -INFINITY) ? 0.f : ex2_approx(mo - mt);
-                        m_used[tid] = mt;
-                        upd = (mo != -INFINITY);
-                    }
-                    alpha_s[tid] = a;
+                    for (int h = 0; h < kH; ++h) x[h] = -INFINITY;
                 }
-                const bool any_upd = named_bar_or(1, 128, upd);
+                // Reference maxima (scaled, log2 units): set from the item's first tile.
+                // Afterwards a head's reference only moves when one of its scores exceeds
+                // it by more than 2^16 (checked per thread; rare), so the common path has
+                // no cross-thread reduction.  The scale is > 0, so maxima of the raw
+                // scores are maxima of the scaled ones.
+                bool need_red = (t == 0);
+                if (!need_red) {
+                    bool viol = false;
+#pragma unroll
+                    for (int h4 = 0; h4 < kH / 4; ++h4) {
+                        const float4 m4 = reinterpret_cast<const float4*>(m_used)[h4];
+                        viol |= x[4 * h4 + 0] * p.scale_log2 > m4.x + kRescaleThreshold;
+                        viol |= x[4 * h4 + 1] * p.scale_log2 > m4.y + kRescaleThreshold;
+                        viol |= x[4 * h4 + 2] * p.scale_log2 > m4.z + kRescaleThreshold;
+                        viol |= x[4 * h4 + 3] * p.scale_log2 > m4.w + kRescaleThreshold;
+                    }
+                    need_red = named_bar_or(1, 128, viol);
+                }
+                bool any_upd = false;
+                if (need_red) {
+                    float r0, r1;
+                    warp_transpose_reduce<true>(x, lane, r0, r1);
+                    red[sw * kH + 2 * lane] = r0;
+                    red[sw * kH + 2 * lane + 1] = r1;
+                    named_bar_sync(1, 128);
+                    bool upd = false;
+                    if (tid < kH) {
+                        const float mt = p.scale_log2 * fmaxf(fmaxf(red[tid], red[kH + tid]),
+                                                              fmaxf(red[2 * kH + tid], red[3 * kH + tid]));
+                        const float mo = m_used[tid];
+                        float a = 1.f;
+                        if (mt > -INFINITY && (mo == -INFINITY || mt > mo + kRescaleThreshold)) {
+                            a = (mo == -INFINITY) ? 0.f : ex2_approx(mo - mt);
+                            m_used[tid] = mt;
+                            upd = (mo != -INFINITY);
+                        }
+                        alpha_s[tid] = a;
+                    }
+                    any_upd = named_bar_or(1, 128, upd);
+                }
                 // probabilities (bf16 for the MMA, float32 for the row sum)
                 uint32_t packed[kH / 2];
 #pragma unroll
@@ -428,10 +451,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const float mm[4] = {m4.x, m4.y, m4.z, m4.w};
                     float pr[4];
 #pragma unroll
-                    for (int k = 0; k < 4; ++k) {
-                        const float mref = (mm[k] == -INFINITY) ? 0.f : mm[k];
-                        pr[k] = ex2_approx(x[4 * h4 + k] - mref);
-                    }
+                    for (int k = 0; k < 4; ++k)
+                        pr[k] = ex2_approx(fmaf(x[4 * h4 + k], p.scale_log2, (mm[k] == -INFINITY) ? 0.f : -mm[k]));
                     if (any_upd) {
                         const float4 a4 = reinterpret_cast<const float4*>(alpha_s)[h4];
                         l_part[4 * h4 + 0] *= a4.x;
