@@ -19,7 +19,8 @@
 //     no per-head [L, N] tensor ever exists.  Each warp then stores 32
 //     consecutive keys of a score row (128-byte coalesced stores).
 //   * Warp roles: warp 0 issues TMA, warp 1 issues the MMAs (one thread), warps
-//     2..5 run the epilogue, one TMEM lane quadrant each.
+//     2..9 run the epilogue, two per TMEM lane quadrant (four of the eight
+//     queries each), reading two queries' 32 head columns per TMEM wait.
 //   * Work items are (batch, 8-query group, key chunk); CTAs are persistent and
 //     walk the items in a zig-zag order so the triangular causal workload of a
 //     first chunk spreads evenly.  Key tiles past the group's last causal key
@@ -41,7 +42,8 @@ namespace {
 constexpr int kHi = DSA_INDEXER_HEADS;  // 32
 constexpr int kDi = DSA_INDEXER_DIM;    // 128
 constexpr int kTileKeys = 128;          // MMA M
-constexpr int kThreads = 192;           // 6 warps
+constexpr int kEpiWarps = 8;            // two per TMEM lane quadrant
+constexpr int kThreads = (2 + kEpiWarps) * 32;   // 320
 
 struct IndexerParams {
     const float* w;
@@ -141,7 +143,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(b_empty, 1);
         for (int a = 0; a < 2; ++a) {
             mbar_init(&acc_full[a], 1);
-            mbar_init(&acc_empty[a], 128);
+            mbar_init(&acc_empty[a], kEpiWarps * 32);
         }
         *abort_flag = 0;
         fence_mbar_init();
@@ -224,8 +226,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         }
     } else {
-        // ------------------------------------------------------------ epilogue (warps 2..5)
+        // ------------------------------------------------------------ epilogue (warps 2..9)
+        // Two warps per TMEM lane quadrant; each takes half of the group's
+        // queries and reads their 32 head columns two queries per TMEM wait.
+        const int e = warp - 2;                      // 0..7
         const int quad = warp & 3;                   // TMEM lane quadrant of this warp
+        constexpr int kPerQuad = kEpiWarps / 4;
+        constexpr int QW = (QG + kPerQuad - 1) / kPerQuad;   // queries per warp (may be none)
+        const int qbase = (e >> 2) * QW;
         const int key_in_tile = quad * 32 + (int)lane;
         const uint32_t lane_addr = static_cast<uint32_t>(quad * 32) << 16;
         int acc_it = 0;
@@ -236,6 +244,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (item < 0) continue;
             Item I = decode_item(p, item, QG);
             const int64_t row0 = (int64_t)I.b * p.L + I.i0;
+            const int q_end = min(qbase + QW, I.nq);     // this warp's queries are [qbase, q_end)
             for (int t = I.t_begin; t < I.t_end; ++t) {
                 const int j = t * kTileKeys + key_in_tile;
                 float* srow = p.scores + row0 * p.ld + j;
@@ -245,29 +254,50 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tc_fence_after();
                     const float4* w4 = reinterpret_cast<const float4*>(p.w + row0 * kHi);
 #pragma unroll 1
-                    for (int q = 0; q < QG; ++q) {
-                        uint32_t v[32];
-                        tmem_ld32(tmem_base + lane_addr + acc * C::N + q * kHi, v);
+                    for (int q = qbase; q < qbase + QW; q += 2) {
+                        if (q >= QG) break;  // warp-uniform: no TMEM columns of this warp's half exist
+                        // two queries per TMEM wait (the pair is always in [0, QG) for QG even)
+                        uint32_t v0[32], v1[32];
+                        tmem_ld32(tmem_base + lane_addr + acc * C::N + q * kHi, v0);
+                        if (QG > 1) tmem_ld32(tmem_base + lane_addr + acc * C::N + (q + 1) * kHi, v1);
                         tmem_ld_wait();
-                        float sacc = 0.f;
-                        if (q < I.nq) {
+                        float a0 = 0.f, b0 = 0.f, a1 = 0.f, b1 = 0.f;
+                        if (q < q_end) {
 #pragma unroll
                             for (int h4 = 0; h4 < kHi / 4; ++h4) {
                                 const float4 wv = __ldg(w4 + q * (kHi / 4) + h4);
-                                sacc = fmaf(wv.x, fmaxf(__uint_as_float(v[4 * h4 + 0]), 0.f), sacc);
-                                sacc = fmaf(wv.y, fmaxf(__uint_as_float(v[4 * h4 + 1]), 0.f), sacc);
-                                sacc = fmaf(wv.z, fmaxf(__uint_as_float(v[4 * h4 + 2]), 0.f), sacc);
-                                sacc = fmaf(wv.w, fmaxf(__uint_as_float(v[4 * h4 + 3]), 0.f), sacc);
+                                a0 = fmaf(wv.x, fmaxf(__uint_as_float(v0[4 * h4 + 0]), 0.f), a0);
+                                b0 = fmaf(wv.y, fmaxf(__uint_as_float(v0[4 * h4 + 1]), 0.f), b0);
+                                a0 = fmaf(wv.z, fmaxf(__uint_as_float(v0[4 * h4 + 2]), 0.f), a0);
+                                b0 = fmaf(wv.w, fmaxf(__uint_as_float(v0[4 * h4 + 3]), 0.f), b0);
                             }
-                            const long long lim = min((long long)I.pos0 + I.i0 + q, (long long)I.kl - 1);
-                            if (j < p.Nmax) srow[(int64_t)q * p.ld] = ((long long)j <= lim) ? sacc : -INFINITY;
+                        }
+                        if (QG > 1 && q + 1 < q_end) {
+#pragma unroll
+                            for (int h4 = 0; h4 < kHi / 4; ++h4) {
+                                const float4 wv = __ldg(w4 + (q + 1) * (kHi / 4) + h4);
+                                a1 = fmaf(wv.x, fmaxf(__uint_as_float(v1[4 * h4 + 0]), 0.f), a1);
+                                b1 = fmaf(wv.y, fmaxf(__uint_as_float(v1[4 * h4 + 1]), 0.f), b1);
+                                a1 = fmaf(wv.z, fmaxf(__uint_as_float(v1[4 * h4 + 2]), 0.f), a1);
+                                b1 = fmaf(wv.w, fmaxf(__uint_as_float(v1[4 * h4 + 3]), 0.f), b1);
+                            }
+                        }
+                        if (j < p.Nmax) {
+                            if (q < q_end) {
+                                const long long lim = min((long long)I.pos0 + I.i0 + q, (long long)I.kl - 1);
+                                srow[(int64_t)q * p.ld] = ((long long)j <= lim) ? a0 + b0 : -INFINITY;
+                            }
+                            if (QG > 1 && q + 1 < q_end) {
+                                const long long lim = min((long long)I.pos0 + I.i0 + q + 1, (long long)I.kl - 1);
+                                srow[(int64_t)(q + 1) * p.ld] = ((long long)j <= lim) ? a1 + b1 : -INFINITY;
+                            }
                         }
                     }
                     tc_fence_before();
                     mbar_arrive(&acc_empty[acc]);
                     ++acc_it;
                 } else if (j < p.Nmax) {
-                    for (int q = 0; q < I.nq; ++q) srow[(int64_t)q * p.ld] = -INFINITY;
+                    for (int q = qbase; q < q_end; ++q) srow[(int64_t)q * p.ld] = -INFINITY;
                 }
             }
         }
