@@ -7,6 +7,11 @@ DSA indexer scores -> top-k selection -> sparse absorbed-MLA attention, the
 three C-ABI calls of libdsa_gb300.so on inputs resident in HBM.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+                    [--workload NAME] [--queries N] [--no-cpu-baseline]
+
+--workload picks another of the seeded workloads (the 4k first chunk, the 64k
+chunk, the 1k tiny chunk, or a decode batch: one new token for each of B
+sequences, through the batched decode entry point, reported in us/step).
 
 Prints one JSON line (rank 0).  Under torchrun each rank processes its own
 chunk on its own GPU (independent problems, no data-path collective), so
@@ -76,7 +81,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.FIELDS,
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", "100"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.thread = threading.Thread(target=self._read, daemon=True)
             self.thread.start()
@@ -117,20 +122,28 @@ class ClockSampler:
 
 # ----------------------------------------------------------------------------- oracle (CPU) timing
 
+def is_decode(wl):
+    """One query per sequence: the batched decode entry point serves it."""
+    return wl.L == 1
+
+
 def oracle_sample(wl, inputs, rows, threads):
-    """Run the float64 oracle chain on the given query rows; return seconds."""
+    """Run the float64 oracle chain on the given query rows (flat b*L+i); return seconds."""
     import oracle
     qi, ki, w, q, kv, q_pos0, kv_len = inputs
     t0 = time.perf_counter()
     S = oracle.indexer(qi, ki, w, q_pos0, kv_len, rows=rows, threads=threads)
     idx = oracle.topk(S.astype(np.float32), q_pos0, kv_len, wl.B, wl.L, wl.top_k, rows=rows, threads=threads)
-    oracle.attention(q[0], kv, idx, np.zeros(wl.L, np.int32), W.SCALE, rows=rows, threads=threads)
+    qf = q.reshape(wl.B * wl.L, q.shape[2], q.shape[3])
+    row_batch = (np.arange(wl.B * wl.L) // wl.L).astype(np.int32)
+    oracle.attention(qf, kv, idx, row_batch, W.SCALE, rows=rows, threads=threads)
     return time.perf_counter() - t0
 
 
 def sample_rows(wl, n, seed):
     rng = np.random.default_rng(seed)
-    return sorted(rng.choice(wl.L, size=min(n, wl.L), replace=False).tolist())
+    R = wl.B * wl.L
+    return sorted(rng.choice(R, size=min(n, R), replace=False).tolist())
 
 
 def run_reference(args, wl, rank, world):
@@ -141,22 +154,28 @@ def run_reference(args, wl, rank, world):
     oracle.build()
     inputs = make_inputs(wl)
     threads = oracle.default_threads()
-    rows_per_step = threads
+    decode = is_decode(wl)
+    rows_per_step = wl.B * wl.L if decode else threads   # decode: the whole batch's new tokens
     for s in range(args.warmup):
         oracle_sample(wl, inputs, sample_rows(wl, rows_per_step, 100 + s), threads)
     tot = 0.0
     for s in range(args.steps):
         tot += oracle_sample(wl, inputs, sample_rows(wl, rows_per_step, 1000 + s), threads)
-    value = rows_per_step * args.steps / tot
+    if decode:
+        metric = f"decode us/step (indexer+top-k+sparse MLA, batch {wl.B}, {wl.N} keys)"
+        value, unit, hib = 1e6 * tot / args.steps, "us/step", False
+        what = f"all {rows_per_step} sequences of the batch per step, {args.steps} steps"
+    else:
+        metric, value, unit, hib = METRIC, rows_per_step * args.steps / tot, UNIT, True
+        what = (f"{rows_per_step} query rows per step (indexer over all causal keys, top-k, attention over "
+                f"{wl.top_k} keys), {args.steps} steps")
     line = {
-        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "impl": "reference", "metric": metric, "value": value, "unit": unit, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * tot / args.steps,
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "higher_is_better": hib, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic", "config": config_block(wl, world),
-        "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
-                         "sample": f"{rows_per_step} query rows per step (indexer over all causal keys, "
-                                   f"top-k, attention over 2048 keys), {args.steps} steps"},
-        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "cpu_baseline": {"value": value, "unit": unit, "cores": threads, "kind": "oracle", "sample": what},
+        "e2e": {"value": value, "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
     return 0
@@ -198,9 +217,17 @@ def run_gpu(args, wl, rank, world, local_rank):
     ld = (wl.N + 3) // 4 * 4
     S = torch.empty((wl.B, wl.L, ld), dtype=torch.float32, device=dev)
     idx = torch.empty((wl.B, wl.L, wl.top_k), dtype=torch.int32, device=dev)
-    out = torch.empty((wl.L, 64, 512), dtype=torch.bfloat16, device=dev)
+    decode = is_decode(wl)
+    out = torch.empty((wl.B if decode else wl.L, 64, 512), dtype=torch.bfloat16, device=dev)
+    ws = torch.empty((dsa.attn_workspace_size(wl.B, wl.top_k),), dtype=torch.uint8, device=dev) if decode else None
     flush = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream()
+
+    def attention(a_q, a_kv, a_len):
+        if decode:   # one query per sequence: the batched decode entry point
+            dsa.mla_sparse_attn_decode(a_q[:, 0], a_kv, a_len, idx[:, 0], W.SCALE, out=out, workspace=ws)
+        else:
+            dsa.mla_sparse_attn_prefill(a_q[0], a_kv[0], idx[0], W.SCALE, out=out)
 
     def step(ev=None):
         if ev:
@@ -211,7 +238,7 @@ def run_gpu(args, wl, rank, world, local_rank):
         dsa.topk(S, dpos, dlen, wl.N, wl.top_k, idx=idx)
         if ev:
             ev[2].record(stream)
-        dsa.mla_sparse_attn_prefill(dq[0], dkv[0], idx[0], W.SCALE, out=out)
+        attention(dq, dkv, dlen)
         if ev:
             ev[3].record(stream)
 
@@ -227,7 +254,11 @@ def run_gpu(args, wl, rank, world, local_rank):
         dist.barrier()
     torch.cuda.synchronize()
     sampler.start()
-    time.sleep(0.3)
+    t_load = time.time() + 0.4       # untimed steps while the clock sampler starts (GPU under the same load)
+    while time.time() < t_load:
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
     for k in range(args.steps):
         flush.zero_()
         step(evs[k])
@@ -247,7 +278,7 @@ def run_gpu(args, wl, rank, world, local_rank):
     # ---- end to end through the public API with host buffers (pinned), copies timed
     host_in = [torch.from_numpy(np.ascontiguousarray(a.view(np.int16) if a.dtype == np.uint16 else a)).pin_memory()
                for a in (qi, ki, w, q_pos0, kv_len, q, kv)]
-    host_out = torch.empty((wl.L, 64, 512), dtype=torch.bfloat16).pin_memory()
+    host_out = torch.empty(tuple(out.shape), dtype=torch.bfloat16).pin_memory()
     dev_in = [h.to(dev) for h in host_in]
     h2d = sum(h.numel() * h.element_size() for h in host_in)
     d2h = host_out.numel() * host_out.element_size()
@@ -258,7 +289,7 @@ def run_gpu(args, wl, rank, world, local_rank):
         a_qi, a_ki, a_w, a_pos, a_len, a_q, a_kv = dev_in
         dsa.indexer_scores(a_qi, a_ki, a_w, a_pos, a_len, scores=S)
         dsa.topk(S, a_pos, a_len, wl.N, wl.top_k, idx=idx)
-        dsa.mla_sparse_attn_prefill(a_q[0], a_kv[0], idx[0], W.SCALE, out=out)
+        attention(a_q, a_kv, a_len)
         host_out.copy_(out, non_blocking=True)
 
     e2e_step()
@@ -294,35 +325,50 @@ def run_gpu(args, wl, rank, world, local_rank):
             traffic = json.load(open(tpath)).get(wl.name, {}).get("mla_sparse_attn")
         except ValueError:
             traffic = None
+    attn_name = "mla_sparse_attn_decode" if decode else "mla_sparse_attn_prefill"
+    hbm = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+    gather_gbs = work["gather_bytes"] / (kern_ms[2] * 1e-3) / 1e9
+    if decode:
+        # decode: a step is one new token for each of the B sequences; time-like metric
+        metric = f"decode us/step (indexer+top-k+sparse MLA, batch {wl.B}, {wl.N} keys)"
+        value, unit, hib = step_ms_max * 1e3, "us/step", False
+        e2e_value = e2e_mean * 1e3
+        roof = {"bound": "hbm", "kernel": attn_name, "achieved": gather_gbs, "peak": hbm, "unit": "GB/s",
+                "frac": gather_gbs / hbm, "traffic": traffic, "peak_kind": f"{peak_kind} HBM copy",
+                "bytes_per_launch": work["gather_bytes"]}
+    else:
+        metric = METRIC
+        value, unit, hib = wl.L * wl.B * world / (step_ms_max * 1e-3), UNIT, True
+        e2e_value = wl.L * wl.B * world / (e2e_mean * 1e-3)
+        roof = {"bound": "tensor", "kernel": attn_name, "achieved": attn_tf, "peak": peak, "unit": "TFLOP/s",
+                "frac": attn_tf / peak, "traffic": traffic, "peak_kind": f"{peak_kind} bf16 dense burst",
+                "flop_per_launch": work["attn_flop"]}
     line = {
-        "metric": METRIC,
-        "value": wl.L * wl.B * world / (step_ms_max * 1e-3),
-        "unit": UNIT,
+        "metric": metric,
+        "value": value,
+        "unit": unit,
         "n_gpus": world,
         "steps": args.steps,
         "warmup": max(3, args.warmup),
         "ms_per_step": step_ms_max,
-        "higher_is_better": True,
+        "higher_is_better": hib,
         "scaling": "weak",
         "vs_baseline": None,
         "dtype": "bf16",
         "data": "synthetic",
         "config": config_block(wl, world),
-        "roofline": {"bound": "tensor", "kernel": "mla_sparse_attn_prefill", "achieved": attn_tf,
-                     "peak": peak, "unit": "TFLOP/s", "frac": attn_tf / peak, "traffic": traffic,
-                     "peak_kind": f"{peak_kind} bf16 dense burst",
-                     "flop_per_launch": work["attn_flop"]},
+        "roofline": roof,
         "kernels_ms": {"dsa_indexer_scores": float(kern_ms[0]), "dsa_topk": float(kern_ms[1]),
-                       "mla_sparse_attn_prefill": float(kern_ms[2])},
+                       attn_name: float(kern_ms[2])},
         "kernel_rooflines": {
             "dsa_indexer_scores": {"bound": "tensor", "achieved_tflops": idx_tf, "frac": idx_tf / peak},
-            "dsa_topk": {"bound": "hbm", "achieved_gbs": topk_gbs,
-                         "frac": topk_gbs / float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))},
-            "mla_sparse_attn_prefill": {"bound": "tensor", "achieved_tflops": attn_tf, "frac": attn_tf / peak},
+            "dsa_topk": {"bound": "hbm", "achieved_gbs": topk_gbs, "frac": topk_gbs / hbm},
+            attn_name: {"bound": "tensor", "achieved_tflops": attn_tf, "frac": attn_tf / peak,
+                        "gather_gbs": gather_gbs, "gather_frac_of_hbm": gather_gbs / hbm},
         },
-        "e2e": {"value": wl.L * wl.B * world / (e2e_mean * 1e-3), "unit": UNIT,
+        "e2e": {"value": e2e_value, "unit": unit,
                 "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)},
-        "gpu_launches": 3 * args.steps,
+        "gpu_launches": (4 if decode else 3) * args.steps,
         "clocks": clocks,
         "device_status": status,
     }
@@ -332,9 +378,14 @@ def run_gpu(args, wl, rank, world, local_rank):
         threads = oracle.default_threads()
         rows = sample_rows(wl, 2 * threads, 7)
         secs = oracle_sample(wl, inputs, rows, threads)
-        line["cpu_baseline"] = {"value": len(rows) / secs, "unit": UNIT, "cores": threads, "kind": "oracle",
-                                "sample": f"{len(rows)} seeded query rows of the same chunk: indexer over all "
-                                          f"their causal keys, top-k, attention over their 2048 keys"}
+        if decode:
+            cpu = {"value": secs * 1e6 * (wl.B / len(rows)), "unit": "us/step"}
+            what = f"all {len(rows)} sequences of the batch: indexer, top-k and attention for each new token"
+        else:
+            cpu = {"value": len(rows) / secs, "unit": UNIT}
+            what = (f"{len(rows)} seeded query rows of the same chunk: indexer over all their causal keys, "
+                    f"top-k, attention over their {wl.top_k} keys")
+        line["cpu_baseline"] = dict(cpu, cores=threads, kind="oracle", sample=what)
     print(json.dumps(line), flush=True)
     return 0
 
@@ -342,7 +393,7 @@ def run_gpu(args, wl, rank, world, local_rank):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(W.WORKLOADS))
@@ -354,8 +405,6 @@ def main():
     if args.queries and args.queries < wl.L:
         wl = W.custom(f"{wl.name}_last{args.queries}", B=wl.B, L=args.queries, p0=wl.N - args.queries, N=wl.N,
                       top_k=wl.top_k, seed=wl.seed, rope_std=wl.rope_std, dup_frac=wl.dup_frac)
-    if wl.name.startswith("decode"):
-        raise SystemExit("bench.py times prefill chunks; decode steps are timed by the decode tests")
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))

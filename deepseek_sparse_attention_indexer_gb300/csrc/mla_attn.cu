@@ -16,18 +16,25 @@
 //     (128 keys x 64 dims per 16 KB block, 9 blocks).  QK reads it K-major;
 //     PV reads the very same bytes as the MN-major V^T operand, so the latent
 //     rows are gathered once and used twice (keys and values).
-//   * Gather: 4 warps issue 16-byte cp.async copies of the selected rows,
-//     straight into the swizzled layout, in 5 segments (4 latent 128-dim
-//     chunks + the rope block).  Each segment has its own full/free barrier so
-//     the next tile's chunk c streams in as soon as PV has consumed chunk c.
-//     Unselected or padding slots are zero-filled (never NaN garbage).
-//   * Softmax: 4 warps, one key per thread.  Each head's reference maximum is
-//     taken from the query's first tile (transposing warp butterfly + one
-//     shared-memory exchange); later tiles only check, per thread, whether a
-//     score exceeds its reference by more than 2^16, and only then reduce and
-//     rescale O^T in TMEM.  Numerator and denominator always share the
-//     reference, so the result is the exact softmax.  P^T is written as bf16
-//     into the (consumed) rope block.
+//   * Sixteen worker warps do both the gather and the softmax.  A worker
+//     warp copies 8 rows of a tile (two per key quarter) with 16-byte
+//     cp.async straight into the swizzled layout.  PV runs one key quarter
+//     at a time and frees each quarter of the stage (its latent rows and
+//     its P^T rows) as soon as it is consumed, so the copies of tile t+1
+//     overlap PV of tile t and only the last quarter's copies sit between
+//     PV(t) and QK(t+1).  The copies of tile t+1 are issued right after the
+//     warp's softmax of tile t, so the whole CTA issues copies (cp.async
+//     throughput from L2 grows with the number of issuing warps).  QK waits
+//     per 128-dim chunk of the K-dim.  Unselected or padding slots are
+//     zero-filled.
+//   * Softmax: four warps per TMEM lane quadrant, 16 heads each, one key per
+//     thread.  Each head's reference maximum is taken from the query's first
+//     tile (transposing warp butterfly + one shared-memory exchange); later
+//     tiles only check, per thread, whether a score exceeds its reference by
+//     more than 2^16, and only then reduce and rescale O^T in TMEM.
+//     Numerator and denominator always share the reference, so the result is
+//     the exact softmax.  P^T is written as bf16 into the (consumed) rope
+//     block.
 //   * The query's Q^T (72 KB) is loaded by TMA once per query.
 //   * Decode splits a sequence's selected keys over CTAs and writes partial
 //     (normalised output, lse) pairs; a small kernel merges them.
@@ -53,7 +60,11 @@ constexpr int kRowBytes = kD * 2;      // 1152
 constexpr int kTile = 128;             // keys per tile (MMA M)
 constexpr int kBlkBytes = kTile * 128; // 16 KB: 128 keys x 64 dims
 constexpr int kQBlkBytes = kH * 128;   // 8 KB: 64 heads x 64 dims
-constexpr int kThreads = 320;          // 10 warps
+constexpr int kWorkerWarps = 16;                  // gather + softmax warps
+constexpr int kWorkers = kWorkerWarps * 32;        // 512
+constexpr int kThreads = 64 + kWorkers;            // warp 0 Q loader, warp 1 MMA, warps 2.. workers
+constexpr int kHG = kH / (kWorkerWarps / 4);       // 16 heads per worker warp
+static_assert(kWorkerWarps == 16 && kTile == 128, "a worker warp copies two rows of each 32-key quarter");
 constexpr float kRescaleThreshold = 16.0f;  // log2 units
 
 // smem layout (1024-aligned base)
@@ -64,8 +75,8 @@ constexpr int OFF_MUSED = OFF_RED + 4 * kH * 4;        // float [64]
 constexpr int OFF_ALPHA = OFF_MUSED + kH * 4;          // float [64]
 constexpr int OFF_INVL = OFF_ALPHA + kH * 4;           // float [64]
 constexpr int OFF_BAR = OFF_INVL + kH * 4;
-// barriers: q_full, q_empty, seg_full[5], seg_free[5], s_full, s_empty, p_full, pv_done
-constexpr int N_BARS = 2 + 5 + 5 + 4;
+// barriers: q_full, q_empty, seg_full[5], qtr_free[4], s_full, s_empty, p_full, pv_done
+constexpr int N_BARS = 2 + 5 + 4 + 4;
 constexpr int OFF_TMEM = OFF_BAR + N_BARS * 8;
 constexpr int OFF_ABORT = OFF_TMEM + 4;
 constexpr int SMEM_BYTES = OFF_ABORT + 4 + 1024;
@@ -94,6 +105,11 @@ struct AttnParams {
     float scale_log2;          // scale * log2(e)
     int32_t* status;           // device error word
 };
+
+// Waits of the worker warps (every lane polls).
+__device__ __forceinline__ bool worker_wait(uint64_t* bar, uint32_t parity, volatile int* abort, int32_t* status) {
+    return mbar_wait(bar, parity, abort, status);
+}
 
 struct Item {
     int row, split, batch, slot0, slot_end, bound;
@@ -134,38 +150,39 @@ __device__ __forceinline__ int item_tiles(const AttnParams& p, const Item& I, ui
     return 0;
 }
 
-// Transposing butterfly over a warp: on entry every lane holds 64 values (one
-// per head); on exit lane l holds the warp-wide reduction for heads 2l, 2l+1.
+// Transposing butterfly over a warp: on entry every lane holds 16 values (one
+// per head of the warp's head group); on exit lanes 2i and 2i+1 hold the
+// warp-wide reduction for head i of the group.
 template <bool MAX>
-__device__ __forceinline__ void warp_transpose_reduce(const float (&x)[64], uint32_t lane, float& r0, float& r1) {
-    float a[32];
+__device__ __forceinline__ float warp_transpose_reduce16(const float (&x)[16], uint32_t lane) {
+    float a[8];
     {
         const bool up = lane & 16;
 #pragma unroll
-        for (int k = 0; k < 32; ++k) {
-            float mine = up ? x[32 + k] : x[k];
-            float other = up ? x[k] : x[32 + k];
-            float recv = __shfl_xor_sync(0xffffffffu, other, 16);
+        for (int k = 0; k < 8; ++k) {
+            const float mine = up ? x[8 + k] : x[k];
+            const float other = up ? x[k] : x[8 + k];
+            const float recv = __shfl_xor_sync(0xffffffffu, other, 16);
             a[k] = MAX ? fmaxf(mine, recv) : mine + recv;
         }
     }
 #pragma unroll
-    for (int step = 0; step < 4; ++step) {
-        const int half = 16 >> step;         // 16, 8, 4, 2 values kept
-        const int off = 8 >> step;           // shuffle distance 8, 4, 2, 1
+    for (int step = 0; step < 3; ++step) {
+        const int half = 4 >> step;   // 4, 2, 1 values kept
+        const int off = 8 >> step;    // shuffle distance 8, 4, 2
         const bool up = lane & off;
 #pragma unroll
-        for (int k = 0; k < 16; ++k) {
+        for (int k = 0; k < 4; ++k) {
             if (k < half) {
-                float mine = up ? a[half + k] : a[k];
-                float other = up ? a[k] : a[half + k];
-                float recv = __shfl_xor_sync(0xffffffffu, other, off);
+                const float mine = up ? a[half + k] : a[k];
+                const float other = up ? a[k] : a[half + k];
+                const float recv = __shfl_xor_sync(0xffffffffu, other, off);
                 a[k] = MAX ? fmaxf(mine, recv) : mine + recv;
             }
         }
     }
-    r0 = a[0];
-    r1 = a[1];
+    const float o = __shfl_xor_sync(0xffffffffu, a[0], 1);
+    return MAX ? fmaxf(a[0], o) : a[0] + o;
 }
 
 template <bool PARTIAL>
@@ -183,11 +200,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t* q_full = bars + 0;
     uint64_t* q_empty = bars + 1;
     uint64_t* seg_full = bars + 2;
-    uint64_t* seg_free = bars + 7;
-    uint64_t* s_full = bars + 12;
-    uint64_t* s_empty = bars + 13;
-    uint64_t* p_full = bars + 14;
-    uint64_t* pv_done = bars + 15;
+    uint64_t* qtr_free = bars + 7;   // key quarter r (rows 32r..32r+31) of the stage consumed by PV
+    uint64_t* s_full = bars + 11;
+    uint64_t* s_empty = bars + 12;
+    uint64_t* p_full = bars + 13;
+    uint64_t* pv_done = bars + 14;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + OFF_TMEM);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + OFF_ABORT);
 
@@ -197,13 +214,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (threadIdx.x == 0) {
         mbar_init(q_full, 1);
         mbar_init(q_empty, 1);
-        for (int c = 0; c < 5; ++c) {
-            mbar_init(&seg_full[c], 128);
-            mbar_init(&seg_free[c], 1);
-        }
+        for (int c = 0; c < 5; ++c) mbar_init(&seg_full[c], kWorkers);  // one cp.async arrival per worker thread
+        for (int r = 0; r < 4; ++r) mbar_init(&qtr_free[r], 1);
         mbar_init(s_full, 1);
-        mbar_init(s_empty, 128);
-        mbar_init(p_full, 128);
+        mbar_init(s_empty, kWorkerWarps);
+        mbar_init(p_full, kWorkerWarps);
         mbar_init(pv_done, 1);
         *abort_flag = 0;
         fence_mbar_init();
@@ -227,7 +242,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (item == -1) break;
                 if (item < 0) continue;
                 const Item I = decode_item(p, item);
-                if (!mbar_wait(q_empty, (qi & 1) ^ 1, abort_flag, p.status)) break;
+                if (!mbar_wait_spin(q_empty, (qi & 1) ^ 1, abort_flag, p.status)) break;
                 ++qi;
                 mbar_arrive_expect_tx(q_full, 9 * kQBlkBytes);
                 const int qrow = I.row * kH;
@@ -245,14 +260,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             const Item I = decode_item(p, item);
             const int T = item_tiles(p, I, lane);
             if (lane == 0) {
-                ok = mbar_wait(q_full, qi & 1, abort_flag, p.status);
+                ok = mbar_wait_spin(q_full, qi & 1, abort_flag, p.status);
                 const uint32_t q_base = smem_u32(sQ);
                 const uint32_t kv_base = smem_u32(sKV);
+                bool q_released = false;
                 for (int t = 0; ok && t < T; ++t, ++gt) {
                     // ---- S^T = K . Q^T over the 576 dims, segment by segment
-                    if (!(ok = mbar_wait(s_empty, (gt & 1) ^ 1, abort_flag, p.status))) break;
+                    if (!(ok = mbar_wait_spin(s_empty, (gt & 1) ^ 1, abort_flag, p.status))) break;
                     for (int c = 0; c < 5 && ok; ++c) {
-                        if (!(ok = mbar_wait(&seg_full[c], gt & 1, abort_flag, p.status))) break;
+                        if (!(ok = mbar_wait_spin(&seg_full[c], gt & 1, abort_flag, p.status))) break;
                         tc_fence_after();
                         const int b_lo = (c < 4) ? 2 * c : 8;
                         const int nb = (c < 4) ? 2 : 1;
@@ -268,140 +284,180 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     if (!ok) break;
                     mma_commit(s_full);
-                    // ---- O^T += V^T . P^T, 128 latent dims per chunk
-                    if (!(ok = mbar_wait(p_full, gt & 1, abort_flag, p.status))) break;
+                    if (t == T - 1) {
+                        mma_commit(q_empty);  // the next query's Q^T may stream in during the last softmax
+                        q_released = true;
+                    }
+                    // ---- O^T += V^T . P^T, 128 latent dims per chunk, one key quarter at a time so
+                    // that the next tile's rows of a quarter stream in as soon as it is consumed
+                    if (!(ok = mbar_wait_spin(p_full, gt & 1, abort_flag, p.status))) break;
                     tc_fence_after();
                     const uint32_t p_base = kv_base + 8 * kBlkBytes;
-                    for (int c = 0; c < 4; ++c) {
+                    for (int r = 0; r < 4; ++r) {
 #pragma unroll
-                        for (int kk = 0; kk < 8; ++kk) {
-                            // A = V^T: MN-major, 64-dim atoms 16 KB apart (LBO), 8-key groups 1 KB apart (SBO)
-                            const uint64_t ad =
-                                sdesc_sw128(kv_base + (2 * c) * kBlkBytes + kk * 2048, kBlkBytes, 1024);
-                            // B = P^T: MN-major, one 64-head atom, 8-key groups 1 KB apart
-                            const uint64_t bd = sdesc_sw128(p_base + kk * 2048, kBlkBytes, 1024);
-                            mma_bf16_ss(tmem_base + TM_O + 64 * c, ad, bd, IDESC_PV, (t > 0 || kk > 0) ? 1u : 0u);
+                        for (int c = 0; c < 4; ++c) {
+#pragma unroll
+                            for (int k2 = 0; k2 < 2; ++k2) {
+                                const int kk = 2 * r + k2;   // 16 keys per K step
+                                // A = V^T: MN-major, 64-dim atoms 16 KB apart (LBO), 8-key groups 1 KB apart (SBO)
+                                const uint64_t ad =
+                                    sdesc_sw128(kv_base + (2 * c) * kBlkBytes + kk * 2048, kBlkBytes, 1024);
+                                // B = P^T: MN-major, one 64-head atom, 8-key groups 1 KB apart
+                                const uint64_t bd = sdesc_sw128(p_base + kk * 2048, kBlkBytes, 1024);
+                                mma_bf16_ss(tmem_base + TM_O + 64 * c, ad, bd, IDESC_PV,
+                                            (t > 0 || kk > 0) ? 1u : 0u);
+                            }
                         }
-                        mma_commit(&seg_free[c]);
+                        mma_commit(&qtr_free[r]);
                     }
-                    mma_commit(&seg_free[4]);
                     mma_commit(pv_done);
                 }
-                if (ok) mma_commit(q_empty);
+                if (ok && !q_released) mma_commit(q_empty);
                 ++qi;
             }
             ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
         }
-    } else if (warp < 6) {
-        // ------------------------------------------------------------ gather (warps 2..5)
-        const int gw = warp - 2;
-        const uint8_t* kv_bytes = reinterpret_cast<const uint8_t*>(p.kv);
-        int gt = 0;
-        bool ok = true;
-        for (int s = 0; ok; ++s) {
-            const int item = nth_item(p, s);
-            if (item == -1) break;
-            if (item < 0) continue;
-            const Item I = decode_item(p, item);
-            const int T = item_tiles(p, I, lane);
-            const int32_t* ir = p.idx + (int64_t)I.row * p.top_k;
-            const uint8_t* kv_batch = kv_bytes + (int64_t)I.batch * p.Nmax * kRowBytes;
-            for (int t = 0; t < T; ++t, ++gt) {
-                // this lane's row of the tile: gw*32 + lane
-                const int slot = I.slot0 + t * kTile + gw * 32 + (int)lane;
-                int j = (slot < I.slot_end) ? __ldg(ir + slot) : -1;
-                if (j >= I.bound) {
-                    raise_dev_error(p.status, DEV_ERR_BOUNDS);
-                    j = -1;
-                }
-                const uint8_t* src_row = (j >= 0) ? kv_batch + (int64_t)j * kRowBytes : kv_bytes;
-                const uint32_t valid_mask = __ballot_sync(0xffffffffu, j >= 0);
-                for (int c = 0; c < 5; ++c) {
-                    ok = __all_sync(0xffffffffu, mbar_wait(&seg_free[c], (gt & 1) ^ 1, abort_flag, p.status));
-                    if (!ok) break;
-                    if (c < 4) {
-                        // 128 dims = 16 chunks of 16 B per row; two rows per warp instruction
-                        const int chunk = lane & 15;
-                        const int blk = 2 * c + (chunk >> 3);
-                        const int cc = chunk & 7;
-#pragma unroll 4
-                        for (int s2 = 0; s2 < 16; ++s2) {
-                            const int rl = 2 * s2 + (int)(lane >> 4);   // row within this warp's 32
-                            const int row = gw * 32 + rl;
-                            const uint8_t* src = reinterpret_cast<const uint8_t*>(
-                                __shfl_sync(0xffffffffu, reinterpret_cast<unsigned long long>(src_row), rl));
-                            const bool v = (valid_mask >> rl) & 1u;
-                            const uint32_t dst =
-                                smem_u32(sKV) + blk * kBlkBytes + row * 128 + ((cc ^ (row & 7)) << 4);
-                            cp_async_16(dst, src + (c * 16 + chunk) * 16, v ? 16u : 0u);
-                        }
-                    } else {
-                        // rope: 64 dims = 8 chunks per row; four rows per warp instruction
-                        const int cc = lane & 7;
-#pragma unroll 4
-                        for (int s2 = 0; s2 < 8; ++s2) {
-                            const int rl = 4 * s2 + (int)(lane >> 3);
-                            const int row = gw * 32 + rl;
-                            const uint8_t* src = reinterpret_cast<const uint8_t*>(
-                                __shfl_sync(0xffffffffu, reinterpret_cast<unsigned long long>(src_row), rl));
-                            const bool v = (valid_mask >> rl) & 1u;
-                            const uint32_t dst =
-                                smem_u32(sKV) + 8 * kBlkBytes + row * 128 + ((cc ^ (row & 7)) << 4);
-                            cp_async_16(dst, src + (64 + cc) * 16, v ? 16u : 0u);
-                        }
-                    }
-                    cp_async_arrive_noinc(&seg_full[c]);
-                }
-                if (!ok) break;
-            }
-        }
-        cp_async_wait_all();
     } else {
-        // ------------------------------------------------------------ softmax + epilogue (warps 6..9)
-        const int sw = warp - 6;                 // 0..3
-        const int quad = warp & 3;               // TMEM lane quadrant
-        const int tid = sw * 32 + (int)lane;     // 0..127
-        const int key = quad * 32 + (int)lane;   // TMEM lane == key row of the tile == dim row of O^T
+        // ------------------------------------------------------------ workers (warps 2..17)
+        const int ww = warp - 2;                  // 0..15
+        const int quad = warp & 3;                // TMEM lane quadrant this warp may access
+        const int hg = ww >> 2;                   // head group: heads h0 .. h0 + 15
+        const int h0 = hg * kHG;
+        const int tid = ww * 32 + (int)lane;      // 0..511
+        const int key = quad * 32 + (int)lane;    // TMEM lane == key row of the tile == dim row of O^T
         const uint32_t lane_addr = static_cast<uint32_t>(quad * 32) << 16;
         uint8_t* pT = sKV + 8 * kBlkBytes;
+        const uint8_t* kv_bytes = reinterpret_cast<const uint8_t*>(p.kv);
+        const uint32_t kv_smem = smem_u32(sKV);
+
+        // Gather cursor: walks this CTA's (item, tile) sequence one tile ahead
+        // of the softmax.  Items without tiles are skipped here.  A worker warp
+        // copies rows 32r + 2ww and 32r + 2ww + 1 of every key quarter r.
+        int g_s = 0, g_T = 0, g_t = 0, g_gt = 0;
+        Item gI{};
+        bool g_valid = false;
+        int g_j = -1;  // lanes 0..7: key of row 32 (lane / 2) + 2 ww + lane % 2 of the cursor's tile
+        auto g_advance_item = [&]() {
+            g_valid = false;
+            for (;;) {
+                const int it = nth_item(p, g_s);
+                if (it == -1) return;
+                ++g_s;
+                if (it < 0) continue;
+                gI = decode_item(p, it);
+                g_T = item_tiles(p, gI, lane);
+                g_t = 0;
+                if (g_T > 0) {
+                    g_valid = true;
+                    return;
+                }
+            }
+        };
+        // Load the cursor tile's row indices early, so that their latency hides
+        // behind the softmax that precedes the copies.
+        auto gather_prep = [&]() {
+            g_j = -1;
+            if (g_valid && lane < 8) {
+                const int slot = gI.slot0 + g_t * kTile + 32 * (int)(lane >> 1) + 2 * ww + (int)(lane & 1);
+                g_j = (slot < gI.slot_end) ? __ldg(p.idx + (int64_t)gI.row * p.top_k + slot) : -1;
+            }
+        };
+        // Issue this warp's copies of the cursor's tile, quarter by quarter as PV
+        // frees them, then advance the cursor.  Returns false if a wait gave up.
+        auto gather_issue = [&]() -> bool {
+            if (!g_valid) return true;
+            int j = g_j;
+            if (j >= gI.bound) {
+                raise_dev_error(p.status, DEV_ERR_BOUNDS);
+                j = -1;
+            }
+            const uint8_t* kv_batch = kv_bytes + (int64_t)gI.batch * p.Nmax * kRowBytes;
+            const uint8_t* src_row = (j >= 0) ? kv_batch + (int64_t)j * kRowBytes : kv_bytes;
+            const uint32_t valid_mask = __ballot_sync(0xffffffffu, j >= 0);
+            bool ok = true;
+            for (int r = 0; r < 4; ++r) {
+                ok = __all_sync(0xffffffffu, worker_wait(&qtr_free[r], (g_gt & 1) ^ 1, abort_flag, p.status));
+                if (!ok) break;
+                // latent: 512 dims = 64 chunks of 16 B per row; lanes 0-15 take the first row, 16-31 the second
+                {
+                    const int i = (int)(lane >> 4);
+                    const int row = 32 * r + 2 * ww + i;
+                    const uint8_t* src = reinterpret_cast<const uint8_t*>(
+                        __shfl_sync(0xffffffffu, reinterpret_cast<unsigned long long>(src_row), 2 * r + i));
+                    const uint32_t nbytes = ((valid_mask >> (2 * r + i)) & 1u) ? 16u : 0u;
+                    const int chunk = lane & 15;
+                    const uint32_t row_off = row * 128 + (((chunk & 7) ^ (row & 7)) << 4);
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        const int blk = 2 * c + (chunk >> 3);
+                        cp_async_16(kv_smem + blk * kBlkBytes + row_off, src + (c * 16 + chunk) * 16, nbytes);
+                        if (r == 3) cp_async_arrive_noinc(&seg_full[c]);
+                    }
+                }
+                // rope: 64 dims = 8 chunks per row; lanes 0-7 the first row, 8-15 the second
+                {
+                    const int i = (int)((lane >> 3) & 1u);
+                    const int row = 32 * r + 2 * ww + i;
+                    const uint8_t* src = reinterpret_cast<const uint8_t*>(
+                        __shfl_sync(0xffffffffu, reinterpret_cast<unsigned long long>(src_row), 2 * r + i));
+                    if (lane < 16) {
+                        const uint32_t nbytes = ((valid_mask >> (2 * r + i)) & 1u) ? 16u : 0u;
+                        const int cc = lane & 7;
+                        cp_async_16(kv_smem + 8 * kBlkBytes + row * 128 + ((cc ^ (row & 7)) << 4),
+                                    src + (64 + cc) * 16, nbytes);
+                    }
+                    if (r == 3) cp_async_arrive_noinc(&seg_full[4]);
+                }
+            }
+            ++g_gt;
+            if (++g_t >= g_T) g_advance_item();
+            gather_prep();
+            return ok;
+        };
+
+        // `gok` is this warp's copy status; it is folded into the next
+        // consensus barrier (bar.red.and over all workers), so every worker
+        // takes the same path out when any wait gives up.
+        g_advance_item();
+        gather_prep();
+        bool gok = gather_issue();
+        bool failed = false;
         int gt = 0;
-        bool ok = true;
-        for (int s = 0; ok; ++s) {
+        for (int s = 0; !failed; ++s) {
             const int item = nth_item(p, s);
             if (item == -1) break;
             if (item < 0) continue;
             const Item I = decode_item(p, item);
             const int T = item_tiles(p, I, lane);
             const int32_t* ir = p.idx + (int64_t)I.row * p.top_k;
-            named_bar_sync(1, 128);  // previous item's readers of m_used / invl are done
+            named_bar_sync(1, kWorkers);  // previous item's readers of m_used / invl are done
             if (tid < kH) m_used[tid] = -INFINITY;
-            float l_part[kH];
+            float l_part[kHG];
 #pragma unroll
-            for (int h = 0; h < kH; ++h) l_part[h] = 0.f;
-            named_bar_sync(1, 128);
+            for (int h = 0; h < kHG; ++h) l_part[h] = 0.f;
+            named_bar_sync(1, kWorkers);
             for (int t = 0; t < T; ++t, ++gt) {
-                ok = named_bar_and(2, 128, mbar_wait(s_full, gt & 1, abort_flag, p.status));
-                if (!ok) break;
+                const int slot = I.slot0 + t * kTile + key;
+                const int j = (slot < I.slot_end) ? __ldg(ir + slot) : -1;  // issued before the wait
+                if (!named_bar_and(2, kWorkers, gok && worker_wait(s_full, gt & 1, abort_flag, p.status))) {
+                    failed = true;
+                    break;
+                }
                 tc_fence_after();
-                float x[kH];
+                float x[kHG];
                 {
-                    uint32_t v0[32], v1[32];
-                    tmem_ld32(tmem_base + lane_addr + TM_S, v0);
-                    tmem_ld32(tmem_base + lane_addr + TM_S + 32, v1);
+                    uint32_t v[kHG];
+                    tmem_ld16(tmem_base + lane_addr + TM_S + h0, v);
                     tmem_ld_wait();
 #pragma unroll
-                    for (int h = 0; h < 32; ++h) {
-                        x[h] = __uint_as_float(v0[h]);
-                        x[32 + h] = __uint_as_float(v1[h]);
-                    }
+                    for (int h = 0; h < kHG; ++h) x[h] = __uint_as_float(v[h]);
                 }
                 tc_fence_before();
-                mbar_arrive(s_empty);
-                const int slot = I.slot0 + t * kTile + key;
-                int j = (slot < I.slot_end) ? __ldg(ir + slot) : -1;
+                __syncwarp();
+                if (lane == 0) mbar_arrive(s_empty);
                 if (!((j >= 0) && (j < I.bound))) {
 #pragma unroll
-                    for (int h = 0; h < kH; ++h) x[h] = -INFINITY;
+                    for (int h = 0; h < kHG; ++h) x[h] = -INFINITY;
                 }
                 // Reference maxima (scaled, log2 units): set from the item's first tile.
                 // Afterwards a head's reference only moves when one of its scores exceeds
@@ -412,22 +468,20 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (!need_red) {
                     bool viol = false;
 #pragma unroll
-                    for (int h4 = 0; h4 < kH / 4; ++h4) {
-                        const float4 m4 = reinterpret_cast<const float4*>(m_used)[h4];
+                    for (int h4 = 0; h4 < kHG / 4; ++h4) {
+                        const float4 m4 = reinterpret_cast<const float4*>(m_used + h0)[h4];
                         viol |= x[4 * h4 + 0] * p.scale_log2 > m4.x + kRescaleThreshold;
                         viol |= x[4 * h4 + 1] * p.scale_log2 > m4.y + kRescaleThreshold;
                         viol |= x[4 * h4 + 2] * p.scale_log2 > m4.z + kRescaleThreshold;
                         viol |= x[4 * h4 + 3] * p.scale_log2 > m4.w + kRescaleThreshold;
                     }
-                    need_red = named_bar_or(1, 128, viol);
+                    need_red = named_bar_or(1, kWorkers, viol);
                 }
                 bool any_upd = false;
                 if (need_red) {
-                    float r0, r1;
-                    warp_transpose_reduce<true>(x, lane, r0, r1);
-                    red[sw * kH + 2 * lane] = r0;
-                    red[sw * kH + 2 * lane + 1] = r1;
-                    named_bar_sync(1, 128);
+                    const float r = warp_transpose_reduce16<true>(x, lane);
+                    if ((lane & 1u) == 0) red[quad * kH + h0 + (int)(lane >> 1)] = r;
+                    named_bar_sync(1, kWorkers);
                     bool upd = false;
                     if (tid < kH) {
                         const float mt = p.scale_log2 * fmaxf(fmaxf(red[tid], red[kH + tid]),
@@ -441,20 +495,20 @@ __global__ void __launch_bounds__(kThreads, 1)
                         }
                         alpha_s[tid] = a;
                     }
-                    any_upd = named_bar_or(1, 128, upd);
+                    any_upd = named_bar_or(1, kWorkers, upd);
                 }
                 // probabilities (bf16 for the MMA, float32 for the row sum)
-                uint32_t packed[kH / 2];
+                uint32_t packed[kHG / 2];
 #pragma unroll
-                for (int h4 = 0; h4 < kH / 4; ++h4) {
-                    const float4 m4 = reinterpret_cast<const float4*>(m_used)[h4];
+                for (int h4 = 0; h4 < kHG / 4; ++h4) {
+                    const float4 m4 = reinterpret_cast<const float4*>(m_used + h0)[h4];
                     const float mm[4] = {m4.x, m4.y, m4.z, m4.w};
                     float pr[4];
 #pragma unroll
                     for (int k = 0; k < 4; ++k)
                         pr[k] = ex2_approx(fmaf(x[4 * h4 + k], p.scale_log2, (mm[k] == -INFINITY) ? 0.f : -mm[k]));
                     if (any_upd) {
-                        const float4 a4 = reinterpret_cast<const float4*>(alpha_s)[h4];
+                        const float4 a4 = reinterpret_cast<const float4*>(alpha_s + h0)[h4];
                         l_part[4 * h4 + 0] *= a4.x;
                         l_part[4 * h4 + 1] *= a4.y;
                         l_part[4 * h4 + 2] *= a4.z;
@@ -465,81 +519,80 @@ __global__ void __launch_bounds__(kThreads, 1)
                     packed[2 * h4] = pack_bf16x2(pr[0], pr[1]);
                     packed[2 * h4 + 1] = pack_bf16x2(pr[2], pr[3]);
                 }
-                // P^T row `key`: 64 heads x bf16 = 128 B, 128-byte swizzle
+                // P^T row `key`, heads h0..h0+15: 16-byte chunks 2hg and 2hg+1 of the swizzled 128-byte row
 #pragma unroll
-                for (int cc = 0; cc < 8; ++cc) {
-                    uint4 v = make_uint4(packed[4 * cc], packed[4 * cc + 1], packed[4 * cc + 2], packed[4 * cc + 3]);
-                    *reinterpret_cast<uint4*>(pT + key * 128 + ((cc ^ (key & 7)) << 4)) = v;
+                for (int i = 0; i < 2; ++i) {
+                    const int chunk = 2 * hg + i;
+                    const uint4 v = make_uint4(packed[4 * i], packed[4 * i + 1], packed[4 * i + 2], packed[4 * i + 3]);
+                    *reinterpret_cast<uint4*>(pT + key * 128 + ((chunk ^ (key & 7)) << 4)) = v;
                 }
                 fence_proxy_async_smem();
                 if (any_upd && t > 0) {
                     // O^T columns of the raised heads: wait for the previous PV, then rescale in TMEM
-                    ok = named_bar_and(2, 128, mbar_wait(pv_done, (gt - 1) & 1, abort_flag, p.status));
-                    if (!ok) break;
+                    if (!named_bar_and(2, kWorkers, worker_wait(pv_done, (gt - 1) & 1, abort_flag, p.status))) {
+                        failed = true;
+                        break;
+                    }
                     tc_fence_after();
+#pragma unroll 1
                     for (int c = 0; c < 4; ++c) {
+                        uint32_t v[kHG];
+                        const uint32_t a = tmem_base + lane_addr + TM_O + 64 * c + h0;
+                        tmem_ld16(a, v);
+                        tmem_ld_wait();
 #pragma unroll
-                        for (int hh = 0; hh < 2; ++hh) {
-                            uint32_t v[32];
-                            const uint32_t a = tmem_base + lane_addr + TM_O + 64 * c + 32 * hh;
-                            tmem_ld32(a, v);
-                            tmem_ld_wait();
-#pragma unroll
-                            for (int k = 0; k < 32; ++k)
-                                v[k] = __float_as_uint(__uint_as_float(v[k]) * alpha_s[32 * hh + k]);
-                            tmem_st32(a, v);
-                        }
+                        for (int k = 0; k < kHG; ++k) v[k] = __float_as_uint(__uint_as_float(v[k]) * alpha_s[h0 + k]);
+                        tmem_st16(a, v);
                     }
                     tmem_st_wait();
                     tc_fence_before();
                 }
-                mbar_arrive(p_full);
+                __syncwarp();
+                if (lane == 0) mbar_arrive(p_full);
+                // copies of the next tile (this item's or the next item's first)
+                gok = gather_issue();
             }
-            if (!ok) break;
+            if (failed) break;
             // ---------------- final: l = sum of partial row sums; out = O^T / l
-            float r0, r1;
-            warp_transpose_reduce<false>(l_part, lane, r0, r1);
-            red[sw * kH + 2 * lane] = r0;
-            red[sw * kH + 2 * lane + 1] = r1;
-            if (T > 0) {
-                ok = named_bar_and(2, 128, mbar_wait(pv_done, (gt - 1) & 1, abort_flag, p.status));
-                if (!ok) break;
-                tc_fence_after();
-            } else {
-                named_bar_sync(1, 128);
+            {
+                const float r = warp_transpose_reduce16<false>(l_part, lane);
+                if ((lane & 1u) == 0) red[quad * kH + h0 + (int)(lane >> 1)] = r;
             }
+            if (!named_bar_and(2, kWorkers,
+                               gok && (T == 0 || worker_wait(pv_done, (gt - 1) & 1, abort_flag, p.status)))) {
+                failed = true;
+                break;
+            }
+            tc_fence_after();
             float lse_h = -INFINITY;
             if (tid < kH) {
                 const float l = red[tid] + red[kH + tid] + red[2 * kH + tid] + red[3 * kH + tid];
                 invl_s[tid] = (l > 0.f) ? 1.f / l : 0.f;
                 lse_h = (l > 0.f) ? (m_used[tid] + log2f(l)) * 0.6931471805599453f : -INFINITY;
             }
-            named_bar_sync(1, 128);
+            named_bar_sync(1, kWorkers);
+#pragma unroll 1
             for (int c = 0; c < 4; ++c) {
-                float o[kH];
+                float o[kHG];
                 if (T > 0) {
-                    uint32_t v0[32], v1[32];
-                    tmem_ld32(tmem_base + lane_addr + TM_O + 64 * c, v0);
-                    tmem_ld32(tmem_base + lane_addr + TM_O + 64 * c + 32, v1);
+                    uint32_t v[kHG];
+                    tmem_ld16(tmem_base + lane_addr + TM_O + 64 * c + h0, v);
                     tmem_ld_wait();
 #pragma unroll
-                    for (int h = 0; h < 32; ++h) {
-                        o[h] = __uint_as_float(v0[h]) * invl_s[h];
-                        o[32 + h] = __uint_as_float(v1[h]) * invl_s[32 + h];
-                    }
+                    for (int h = 0; h < kHG; ++h) o[h] = __uint_as_float(v[h]) * invl_s[h0 + h];
                 } else {
 #pragma unroll
-                    for (int h = 0; h < kH; ++h) o[h] = 0.f;
+                    for (int h = 0; h < kHG; ++h) o[h] = 0.f;
                 }
                 const int dim = c * 128 + key;
                 if (PARTIAL) {
-                    float* dst = p.part_o + ((int64_t)I.row * p.nsplit + I.split) * kH * kDv + dim;
+                    float* dst = p.part_o + (((int64_t)I.row * p.nsplit + I.split) * kH + h0) * kDv + dim;
 #pragma unroll
-                    for (int h = 0; h < kH; ++h) dst[h * kDv] = o[h];
+                    for (int h = 0; h < kHG; ++h) dst[h * kDv] = o[h];
                 } else {
-                    __nv_bfloat16* dst = p.out + (int64_t)I.row * kH * kDv + dim;
+                    __nv_bfloat16* dst = p.out + ((int64_t)I.row * kH + h0) * kDv + dim;
 #pragma unroll
-                    for (int h = 0; h < kH; ++h) dst[h * kDv] = __float2bfloat16_rn(o[h]);
+                    for (int h = 0; h < kHG; ++h) dst[h * kDv] = __float2bfloat16_rn(o[h]);
                 }
             }
             if (tid < kH) {
@@ -550,6 +603,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             tc_fence_before();
         }
+        cp_async_wait_all();
     }
 
     tc_fence_before();
