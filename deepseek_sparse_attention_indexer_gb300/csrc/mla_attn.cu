@@ -186,7 +186,7 @@ __device__ __forceinline__ float warp_transpose_reduce16(const float (&x)[16], u
 }
 
 template <bool PARTIAL>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreads, 1)   // 18 warps: at most 96 registers a thread (5 warps share one 16K-register SM sub-partition)
     mla_sparse_attn_kernel(const __grid_constant__ CUtensorMap tmap_q, const AttnParams p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -415,9 +415,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             return ok;
         };
 
-        // `gok` is this warp's copy status; it is folded into the next
-        // consensus barrier (bar.red.and over all workers), so every worker
-        // takes the same path out when any wait gives up.
+        // `gok` is this thread's wait status.  A wait that gives up (it also sets
+        // the CTA's abort flag, so every later wait returns at once) does not
+        // change the control flow inside an item: all workers keep meeting the
+        // same named barriers, and the consensus barrier (bar.red.and over all
+        // workers) at the end of the item takes every worker out together.
         g_advance_item();
         gather_prep();
         bool gok = gather_issue();
@@ -439,10 +441,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int t = 0; t < T; ++t, ++gt) {
                 const int slot = I.slot0 + t * kTile + key;
                 const int j = (slot < I.slot_end) ? __ldg(ir + slot) : -1;  // issued before the wait
-                if (!named_bar_and(2, kWorkers, gok && worker_wait(s_full, gt & 1, abort_flag, p.status))) {
-                    failed = true;
-                    break;
-                }
+                gok = gok && worker_wait(s_full, gt & 1, abort_flag, p.status);
                 tc_fence_after();
                 float x[kHG];
                 {
@@ -529,10 +528,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 fence_proxy_async_smem();
                 if (any_upd && t > 0) {
                     // O^T columns of the raised heads: wait for the previous PV, then rescale in TMEM
-                    if (!named_bar_and(2, kWorkers, worker_wait(pv_done, (gt - 1) & 1, abort_flag, p.status))) {
-                        failed = true;
-                        break;
-                    }
+                    gok = gok && worker_wait(pv_done, (gt - 1) & 1, abort_flag, p.status);
                     tc_fence_after();
 #pragma unroll 1
                     for (int c = 0; c < 4; ++c) {
@@ -550,9 +546,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 __syncwarp();
                 if (lane == 0) mbar_arrive(p_full);
                 // copies of the next tile (this item's or the next item's first)
-                gok = gather_issue();
+                gok = gather_issue() && gok;
             }
-            if (failed) break;
             // ---------------- final: l = sum of partial row sums; out = O^T / l
             {
                 const float r = warp_transpose_reduce16<false>(l_part, lane);
