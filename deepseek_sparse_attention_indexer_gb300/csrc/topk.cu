@@ -6,7 +6,7 @@
 // pages leave open: equal scores rank the lower key index first, -0.0 equals
 // +0.0, the selection is written in ascending key order and unused slots hold -1.
 //
-// How: one CTA per score row runs an exact radix select in shared memory.
+// How: one CTA per score row runs an exact radix select.
 //   * Scores map to order-preserving 32-bit keys (-0.0 folded onto +0.0).
 //   * Up to three histogram passes (12 + 12 + 8 bits, shared-memory atomics)
 //     narrow down the threshold key T and how many keys equal to T are still
@@ -15,7 +15,14 @@
 //     with block-wide prefix sums: every key above T, plus the first `need`
 //     keys equal to T (this is the lower-index tie rule).  Positions come from
 //     the prefix sums, so the output is ascending without a sort.
-//   * The first pass reads the row from HBM; later passes hit L2.
+//   * Calls with 8192 < Nmax <= 16384: a thread holds a contiguous run of 32
+//     keys of the row in registers, loaded once from HBM with all of its loads
+//     in flight, for every pass; one block scan orders the compaction.  Two
+//     CTAs per SM.
+//   * Other sizes stream the row on every pass (the first pass reads HBM, later
+//     passes mostly hit L2) with four CTAs per SM: the passes are latency
+//     bound, and more rows in flight win for short rows, while long rows do
+//     not fit in registers.
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -105,7 +112,41 @@ __device__ void find_bin(const uint32_t* hist, int nbins, uint32_t need, uint32_
     __syncthreads();
 }
 
-__global__ void __launch_bounds__(kThreads) topk_kernel(const TopkParams p) {
+// Number of causal keys of score row r (query i of batch b at q_pos0[b] + i).
+__device__ __forceinline__ int row_keys(const TopkParams& p, int r) {
+    const int b = r / p.L, i = r % p.L;
+    const long long pos = (long long)__ldg(p.q_pos0 + b) + i;
+    const long long kl = min((long long)__ldg(p.kv_len + b), (long long)p.Nmax);
+    return (int)max(0LL, min(pos + 1, kl));
+}
+
+constexpr int kPer = 32;                        // keys a thread holds: a contiguous run of the row
+constexpr int kChunk = kThreads * kPer;         // 16384 keys: one block-wide chunk of the row
+// Below this many keys a row is short enough that four streaming CTAs per SM
+// (more rows in flight) beat two register-resident ones (measured on GB300).
+constexpr int kRegMinKeys = 8192;
+
+// Load this thread's run of chunk `ch` of the row (keys 32 t .. 32 t + 31 of
+// the chunk) as order keys; positions past the row get key 0 (no finite or
+// infinite score maps to 0).  The eight float4 loads are issued together and
+// go through L1, which keeps the 128-byte lines the warp's strided accesses touch.
+__device__ __forceinline__ void load_run(const float4* row4, int n, int ch, uint32_t (&key)[kPer]) {
+    const int v0 = (ch * kChunk) / 4 + threadIdx.x * (kPer / 4);
+    const int n4 = (n + 3) / 4;
+    float4 f[kPer / 4];
+#pragma unroll
+    for (int c = 0; c < kPer / 4; ++c) f[c] = (v0 + c < n4) ? __ldg(row4 + v0 + c) : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int c = 0; c < kPer / 4; ++c) {
+        const float e[4] = {f[c].x, f[c].y, f[c].z, f[c].w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) key[4 * c + k] = (4 * (v0 + c) + k < n) ? order_key(e[k]) : 0u;
+    }
+}
+
+// Streaming select (any row length): four CTAs per SM; every pass reads the
+// row again (the first from HBM, later ones mostly from L2).
+__global__ void __launch_bounds__(kThreads, 4) topk_stream_kernel(const TopkParams p) {
     __shared__ uint32_t hist[kBins];
     __shared__ uint32_t warp_sums[kWarps + 1];
     __shared__ uint32_t sel[3];
@@ -200,14 +241,102 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(const TopkParams p) {
     }
 }
 
+// Register-resident select for rows of up to one chunk (16384 keys): the row
+// is loaded once and stays in registers for every pass (two CTAs per SM).
+__global__ void __launch_bounds__(kThreads, 2) topk_reg_kernel(const TopkParams p) {
+    __shared__ uint32_t hist[kBins];
+    __shared__ uint32_t warp_sums[kWarps + 1];
+    __shared__ uint32_t sel[3];
+
+    const int R = p.B * p.L;
+    for (int r = blockIdx.x; r < R; r += gridDim.x) {
+        const int n = row_keys(p, r);
+        int32_t* out = p.idx + (int64_t)r * p.K;
+        if (n <= p.K) {
+            for (int t = threadIdx.x; t < p.K; t += kThreads) out[t] = t < n ? t : -1;
+            continue;
+        }
+        const float4* row4 = reinterpret_cast<const float4*>(p.scores + (int64_t)r * p.ld);
+        uint32_t key[kPer];
+        load_run(row4, n, 0, key);
+
+        // ---- radix narrowing: (shift, prefix, need) describe the threshold class
+        int shift = 32;        // keys compared on bits [shift, 32); 32 = nothing fixed yet
+        uint32_t prefix = 0;
+        uint32_t need = (uint32_t)p.K;
+        const int digit_bits[3] = {12, 12, 8};
+        for (int pass = 0; pass < 3; ++pass) {
+            const int bits = digit_bits[pass];
+            const int nbins = 1 << bits;
+            const int new_shift = shift - bits;
+            for (int k = threadIdx.x; k < nbins; k += kThreads) hist[k] = 0u;
+            __syncthreads();
+#pragma unroll
+            for (int k = 0; k < kPer; ++k) {
+                const uint32_t kk = key[k];
+                const bool in_class = (shift == 32) || ((kk >> shift) == prefix);
+                if (kk != 0u && in_class) atomicAdd(&hist[(kk >> new_shift) & (uint32_t)(nbins - 1)], 1u);
+            }
+            __syncthreads();
+            find_bin(hist, nbins, need, warp_sums, sel);
+            const uint32_t bin = sel[0], rem = sel[1], cnt = sel[2];
+            prefix = (shift == 32 ? 0u : (prefix << bits)) | bin;
+            shift = new_shift;
+            need = rem;
+            __syncthreads();
+            if (rem == cnt) break;  // the whole threshold bucket is taken
+        }
+
+        // ---- ordered compaction: keys above the class, then the first `need` of the class.
+        // One block scan orders every thread's contiguous run.
+        {
+            uint32_t gmask = 0, emask = 0;
+#pragma unroll
+            for (int k = 0; k < kPer; ++k) {
+                const uint32_t kk = key[k];
+                const uint32_t sk = kk >> shift;
+                if (kk != 0u && sk > prefix) gmask |= 1u << k;
+                else if (kk != 0u && sk == prefix) emask |= 1u << k;
+            }
+            const uint32_t packed = ((uint32_t)__popc(emask) << 16) | (uint32_t)__popc(gmask);
+            uint32_t total;
+            const uint32_t pre = block_excl_scan(packed, warp_sums, &total);
+            (void)total;
+            uint32_t g_before = pre & 0xFFFFu;
+            uint32_t e_before = pre >> 16;
+            const int j0 = threadIdx.x * kPer;
+            while (gmask | emask) {
+                const int k = __ffs(gmask | emask) - 1;
+                const uint32_t bit = 1u << k;
+                if (gmask & bit) {
+                    const uint32_t pos = g_before + min(need, e_before);
+                    if (pos < (uint32_t)p.K) out[pos] = j0 + k;
+                    ++g_before;
+                } else {
+                    if (e_before < need && g_before + e_before < (uint32_t)p.K) out[g_before + e_before] = j0 + k;
+                    ++e_before;
+                }
+                gmask &= ~bit;
+                emask &= ~bit;
+            }
+        }
+        __syncthreads();
+    }
+}
+
 }  // namespace
 
 dsa_status_t launch_topk(const float* scores, int64_t ld, const int32_t* q_pos0, const int32_t* kv_len, int B,
                          int L, int Nmax, int top_k, int32_t* idx, cudaStream_t stream) {
     TopkParams p{scores, ld, q_pos0, kv_len, idx, B, L, Nmax, top_k};
     const long long R = (long long)B * L;
-    const int grid = (int)min(R, (long long)device_sm_count() * 4);
-    topk_kernel<<<grid, kThreads, 0, stream>>>(p);
+    if (Nmax > kRegMinKeys && Nmax <= kChunk) {
+        const int grid = (int)min(R, (long long)device_sm_count() * 2);
+        topk_reg_kernel<<<grid, kThreads, 0, stream>>>(p);
+    } else {
+        const int grid = (int)min(R, (long long)device_sm_count() * 4);
+        topk_stream_kernel<<<grid, kThreads, 0, stream>>>(p);
+    }
     return cudaGetLastError() == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
 }
 

@@ -110,8 +110,11 @@ def test_indexer_full_size_sampled(dsa, oracle_mod, name):
 
 # ----------------------------------------------------------------------------- top-k
 
+# Calls with 8192 < Nmax <= 16384 take the register-resident kernel, other sizes the streaming one.
 @pytest.mark.parametrize("rows,n,K,p0", [(64, 5000, 100, 4936), (33, 3000, 2048, 0), (16, 70000, 2048, 69984),
-                                         (40, 2100, 2048, 2000), (8, 300, 1, 292)])
+                                         (40, 2100, 2048, 2000), (8, 300, 1, 292),
+                                         (48, 12000, 2048, 11952), (24, 16384, 2048, 16360),
+                                         (41, 9001, 2048, 8960), (30, 16000, 1, 15970), (6, 10000, 2048, 0)])
 def test_topk_bit_exact_with_ties(dsa, oracle_mod, rows, n, K, p0):
     S = W.random_scores(rows, n, seed=rows * 7 + K)
     q_pos0 = np.array([p0], np.int32)
@@ -125,8 +128,9 @@ def test_topk_bit_exact_with_ties(dsa, oracle_mod, rows, n, K, p0):
     np.testing.assert_array_equal(idx.cpu().numpy()[0], ref)
 
 
-def test_topk_all_equal_and_signed_zero(dsa, oracle_mod):
-    n, K, rows = 4000, 2048, 3
+@pytest.mark.parametrize("n", [4000, 12000])
+def test_topk_all_equal_and_signed_zero(dsa, oracle_mod, n):
+    K, rows = 2048, 3
     S = np.zeros((rows, n), np.float32)
     S[1, ::2] = -0.0
     S[2] = 1.5
