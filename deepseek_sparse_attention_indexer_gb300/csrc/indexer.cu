@@ -19,8 +19,10 @@
 //     no per-head [L, N] tensor ever exists.  Each warp then stores 32
 //     consecutive keys of a score row (128-byte coalesced stores).
 //   * Warp roles: warp 0 issues TMA, warp 1 issues the MMAs (one thread), warps
-//     2..9 run the epilogue, two per TMEM lane quadrant (four of the eight
-//     queries each), reading two queries' 32 head columns per TMEM wait.
+//     2..17 run the epilogue, four per TMEM lane quadrant (two of the eight
+//     queries each, one query's 32 head columns per TMEM wait): with four
+//     epilogue warps per scheduler, one warp's TMEM and weight loads hide
+//     behind the others' arithmetic.
 //   * Work items are (batch, 8-query group, key chunk); CTAs are persistent and
 //     walk the items in a zig-zag order so the triangular causal workload of a
 //     first chunk spreads evenly.  Key tiles past the group's last causal key
@@ -42,8 +44,9 @@ namespace {
 constexpr int kHi = DSA_INDEXER_HEADS;  // 32
 constexpr int kDi = DSA_INDEXER_DIM;    // 128
 constexpr int kTileKeys = 128;          // MMA M
-constexpr int kEpiWarps = 8;            // two per TMEM lane quadrant
-constexpr int kThreads = (2 + kEpiWarps) * 32;   // 320
+constexpr int kEpiWarps = 16;           // four per TMEM lane quadrant
+constexpr int kQPerWait = (kEpiWarps >= 16) ? 1 : 2;   // queries whose TMEM columns one wait covers
+constexpr int kThreads = (2 + kEpiWarps) * 32;   // 576: 18 warps, at most 96 registers a thread
 
 struct IndexerParams {
     const float* w;
@@ -78,6 +81,25 @@ struct Cfg {
     static constexpr int SMEM = OFF_ABORT + 4 + 1024;  // + slack for 1024-byte alignment
     static constexpr uint32_t IDESC = idesc_bf16_f32(kTileKeys, N, false, false);
 };
+
+// One query's score for this thread's key: sum over the 32 heads of
+// w[h] * relu(x[h]), x = the head's 32 TMEM columns.  Even heads accumulate in
+// .x and odd heads in .y of a packed f32x2 FMA; the two halves are added last.
+__device__ __forceinline__ float weighted_relu_sum(const uint32_t (&x)[32], const float4* wq) {
+    float2 s = make_float2(0.f, 0.f);
+#pragma unroll
+    for (int h4 = 0; h4 < kHi / 4; ++h4) {
+        const float4 wv = __ldg(wq + h4);
+        s = __ffma2_rn(make_float2(wv.x, wv.y),
+                       make_float2(fmaxf(__uint_as_float(x[4 * h4 + 0]), 0.f), fmaxf(__uint_as_float(x[4 * h4 + 1]), 0.f)),
+                       s);
+        s = __ffma2_rn(make_float2(wv.z, wv.w),
+                       make_float2(fmaxf(__uint_as_float(x[4 * h4 + 2]), 0.f), fmaxf(__uint_as_float(x[4 * h4 + 3]), 0.f)),
+                       s);
+        asm volatile("" ::: "memory");   // keep each weight load next to its use (register pressure)
+    }
+    return s.x + s.y;
+}
 
 struct Item {
     int b, i0, nq, t_begin, t_end, n_comp_end;  // compute tiles are [t_begin, n_comp_end)
@@ -170,7 +192,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (item < 0) continue;
                 Item I = decode_item(p, item, QG);
                 if (I.n_comp_end <= I.t_begin) continue;
-                if (!(ok = mbar_wait(b_empty, (bi & 1) ^ 1, abort_flag, p.status))) break;
+                if (!(ok = mbar_wait_spin(b_empty, (bi & 1) ^ 1, abort_flag, p.status))) break;
                 ++bi;
                 mbar_arrive_expect_tx(b_full, C::B_BYTES);
                 const int qrow = (I.b * p.L + I.i0) * kHi;
@@ -178,7 +200,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tma_load_2d(sB + C::B_HALF, &tmap_q, b_full, 64, qrow);
                 for (int t = I.t_begin; t < I.n_comp_end; ++t, ++it) {
                     const int st = it % STAGES;
-                    if (!(ok = mbar_wait(&a_empty[st], ((it / STAGES) & 1) ^ 1, abort_flag, p.status))) break;
+                    if (!(ok = mbar_wait_spin(&a_empty[st], ((it / STAGES) & 1) ^ 1, abort_flag, p.status))) break;
                     mbar_arrive_expect_tx(&a_full[st], C::A_BYTES);
                     const int krow = I.b * p.Nmax + t * kTileKeys;
                     uint8_t* dst = sA + st * C::A_BYTES;
@@ -198,15 +220,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (item < 0) continue;
                 Item I = decode_item(p, item, QG);
                 if (I.n_comp_end <= I.t_begin) continue;
-                if (!(ok = mbar_wait(b_full, bi & 1, abort_flag, p.status))) break;
+                if (!(ok = mbar_wait_spin(b_full, bi & 1, abort_flag, p.status))) break;
                 ++bi;
                 tc_fence_after();
                 const uint32_t b_base = smem_u32(sB);
                 for (int t = I.t_begin; t < I.n_comp_end; ++t, ++it, ++acc_it) {
                     const int st = it % STAGES;
                     const int acc = acc_it & 1;
-                    if (!(ok = mbar_wait(&a_full[st], (it / STAGES) & 1, abort_flag, p.status))) break;
-                    if (!(ok = mbar_wait(&acc_empty[acc], ((acc_it >> 1) & 1) ^ 1, abort_flag, p.status))) break;
+                    if (!(ok = mbar_wait_spin(&a_full[st], (it / STAGES) & 1, abort_flag, p.status))) break;
+                    if (!(ok = mbar_wait_spin(&acc_empty[acc], ((acc_it >> 1) & 1) ^ 1, abort_flag, p.status))) break;
                     tc_fence_after();
                     const uint32_t a_base = smem_u32(sA + st * C::A_BYTES);
                     const uint32_t d = tmem_base + acc * C::N;
@@ -227,9 +249,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else {
         // ------------------------------------------------------------ epilogue (warps 2..9)
-        // Two warps per TMEM lane quadrant; each takes half of the group's
-        // queries and reads their 32 head columns two queries per TMEM wait.
-        const int e = warp - 2;                      // 0..7
+        // kEpiWarps / 4 warps per TMEM lane quadrant; each takes its share of the
+        // group's queries and reads kQPerWait queries' 32 head columns per TMEM wait.
+        const int e = warp - 2;                      // 0..kEpiWarps-1
         const int quad = warp & 3;                   // TMEM lane quadrant of this warp
         constexpr int kPerQuad = kEpiWarps / 4;
         constexpr int QW = (QG + kPerQuad - 1) / kPerQuad;   // queries per warp (may be none)
@@ -254,42 +276,28 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tc_fence_after();
                     const float4* w4 = reinterpret_cast<const float4*>(p.w + row0 * kHi);
 #pragma unroll 1
-                    for (int q = qbase; q < qbase + QW; q += 2) {
-                        if (q >= QG) break;  // warp-uniform: no TMEM columns of this warp's half exist
-                        // two queries per TMEM wait (the pair is always in [0, QG) for QG even)
-                        uint32_t v0[32], v1[32];
+                    for (int q = qbase; q < qbase + QW; q += kQPerWait) {
+                        if (q >= QG) break;  // warp-uniform: no TMEM columns of this warp's share exist
+                        // kQPerWait queries' 32 head columns per TMEM wait
+                        uint32_t v0[32], v1[32];   // v1 unused (and eliminated) when one query per wait
                         tmem_ld32(tmem_base + lane_addr + acc * C::N + q * kHi, v0);
-                        if (QG > 1) tmem_ld32(tmem_base + lane_addr + acc * C::N + (q + 1) * kHi, v1);
-                        tmem_ld_wait();
-                        float a0 = 0.f, b0 = 0.f, a1 = 0.f, b1 = 0.f;
-                        if (q < q_end) {
-#pragma unroll
-                            for (int h4 = 0; h4 < kHi / 4; ++h4) {
-                                const float4 wv = __ldg(w4 + q * (kHi / 4) + h4);
-                                a0 = fmaf(wv.x, fmaxf(__uint_as_float(v0[4 * h4 + 0]), 0.f), a0);
-                                b0 = fmaf(wv.y, fmaxf(__uint_as_float(v0[4 * h4 + 1]), 0.f), b0);
-                                a0 = fmaf(wv.z, fmaxf(__uint_as_float(v0[4 * h4 + 2]), 0.f), a0);
-                                b0 = fmaf(wv.w, fmaxf(__uint_as_float(v0[4 * h4 + 3]), 0.f), b0);
-                            }
+                        if constexpr (kQPerWait == 2) {
+                            if (QG > 1) tmem_ld32(tmem_base + lane_addr + acc * C::N + (q + 1) * kHi, v1);
                         }
-                        if (QG > 1 && q + 1 < q_end) {
-#pragma unroll
-                            for (int h4 = 0; h4 < kHi / 4; ++h4) {
-                                const float4 wv = __ldg(w4 + (q + 1) * (kHi / 4) + h4);
-                                a1 = fmaf(wv.x, fmaxf(__uint_as_float(v1[4 * h4 + 0]), 0.f), a1);
-                                b1 = fmaf(wv.y, fmaxf(__uint_as_float(v1[4 * h4 + 1]), 0.f), b1);
-                                a1 = fmaf(wv.z, fmaxf(__uint_as_float(v1[4 * h4 + 2]), 0.f), a1);
-                                b1 = fmaf(wv.w, fmaxf(__uint_as_float(v1[4 * h4 + 3]), 0.f), b1);
-                            }
+                        tmem_ld_wait();
+                        const float r0 = (q < q_end) ? weighted_relu_sum(v0, w4 + q * (kHi / 4)) : 0.f;
+                        float r1 = 0.f;
+                        if constexpr (kQPerWait == 2) {
+                            if (QG > 1 && q + 1 < q_end) r1 = weighted_relu_sum(v1, w4 + (q + 1) * (kHi / 4));
                         }
                         if (j < p.Nmax) {
                             if (q < q_end) {
                                 const long long lim = min((long long)I.pos0 + I.i0 + q, (long long)I.kl - 1);
-                                srow[(int64_t)q * p.ld] = ((long long)j <= lim) ? a0 + b0 : -INFINITY;
+                                srow[(int64_t)q * p.ld] = ((long long)j <= lim) ? r0 : -INFINITY;
                             }
-                            if (QG > 1 && q + 1 < q_end) {
+                            if (kQPerWait == 2 && QG > 1 && q + 1 < q_end) {
                                 const long long lim = min((long long)I.pos0 + I.i0 + q + 1, (long long)I.kl - 1);
-                                srow[(int64_t)(q + 1) * p.ld] = ((long long)j <= lim) ? a1 + b1 : -INFINITY;
+                                srow[(int64_t)(q + 1) * p.ld] = ((long long)j <= lim) ? r1 : -INFINITY;
                             }
                         }
                     }
