@@ -275,6 +275,38 @@ def run_gpu(args, wl, rank, world, local_rank):
     step_ms_max = float(t.item())
     status = dsa.device_status()
 
+    # ---- the same step replayed as one CUDA graph (launch gaps removed); for
+    # decode, where the kernels are microseconds long, this is the step time a
+    # serving loop that captures its decode step sees
+    graph_ms = None
+    try:
+        g = torch.cuda.CUDAGraph()
+        side = torch.cuda.Stream(device=dev)
+        side.wait_stream(stream)
+        with torch.cuda.stream(side):
+            step()                          # warm the library's per-kernel setup on this stream
+        stream.wait_stream(side)
+        torch.cuda.synchronize()
+        with torch.cuda.graph(g):
+            step()
+        for _ in range(3):
+            g.replay()
+        torch.cuda.synchronize()
+        reps = max(20, args.steps)
+        g0 = torch.cuda.Event(enable_timing=True)
+        g1 = torch.cuda.Event(enable_timing=True)
+        g0.record(stream)
+        for _ in range(reps):
+            g.replay()
+        g1.record(stream)
+        torch.cuda.synchronize()
+        graph_ms = g0.elapsed_time(g1) / reps
+        del g
+    except RuntimeError as exc:            # capture unsupported here: report why, keep the line
+        graph_ms = f"unavailable: {exc}"
+    if dsa.device_status() != 0:
+        raise RuntimeError("device error word set during the graph replays")
+
     # ---- end to end through the public API with host buffers (pinned), copies timed
     host_in = [torch.from_numpy(np.ascontiguousarray(a.view(np.int16) if a.dtype == np.uint16 else a)).pin_memory()
                for a in (qi, ki, w, q_pos0, kv_len, q, kv)]
@@ -368,6 +400,9 @@ def run_gpu(args, wl, rank, world, local_rank):
         },
         "e2e": {"value": e2e_value, "unit": unit,
                 "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)},
+        "graph": ({"ms_per_step": graph_ms, "note": "the step replayed as one CUDA graph, inputs resident, "
+                   "no L2 flush between replays"} if isinstance(graph_ms, float) else {"ms_per_step": None,
+                                                                                     "note": graph_ms}),
         "gpu_launches": (4 if decode else 3) * args.steps,
         "clocks": clocks,
         "device_status": status,

@@ -243,3 +243,45 @@ def test_attention_out_of_range_index_is_reported(dsa, oracle_mod):
     skipped[1, 7] = -1
     o_ref, _ = oracle_mod.attention(q[0], kv, skipped, np.zeros(4, np.int32), W.SCALE)
     attn_close(out.float().cpu().numpy(), o_ref, "oob")
+
+
+def run_decode_chain(dsa, oracle_mod, wl, kv_len):
+    """Decode step for B sequences with their own cache lengths (kv_len[b] <= Nmax); each new
+    token sits at position kv_len[b] - 1 and sees all of its sequence's keys."""
+    qi, ki, w = W.make_indexer_inputs(wl)
+    q, kv = W.make_attention_inputs(wl)
+    kv_len = np.asarray(kv_len, np.int32)
+    q_pos0 = kv_len - 1
+    d_pos, d_len = dev(q_pos0), dev(kv_len)
+    S = dsa.indexer_scores(dev(qi), dev(ki), dev(w), d_pos, d_len)
+    idx = dsa.topk(S, d_pos, d_len, wl.N, wl.top_k)
+    out, lse = dsa.mla_sparse_attn_decode(dev(q[:, 0]), dev(kv), d_len, idx[:, 0], W.SCALE, want_lse=True)
+    torch.cuda.synchronize()
+    th = oracle_mod.default_threads()
+    S_ref = oracle_mod.indexer(qi, ki, w, q_pos0, kv_len, threads=th)
+    # scores past a sequence's cache are -inf and never selected
+    got_S = S[:, 0, : wl.N].cpu().numpy().astype(np.float64)
+    np.testing.assert_array_equal(got_S, S_ref.reshape(wl.B, wl.N))
+    idx_ref = oracle_mod.topk(S_ref.astype(np.float32), q_pos0, kv_len, wl.B, 1, wl.top_k, threads=th)
+    np.testing.assert_array_equal(idx[:, 0].cpu().numpy(), idx_ref)
+    o_ref, l_ref = oracle_mod.attention(q[:, 0], kv, idx_ref, np.arange(wl.B, dtype=np.int32), W.SCALE, threads=th)
+    attn_close(out.float().cpu().numpy(), o_ref, wl.name)
+    np.testing.assert_allclose(lse.cpu().numpy(), l_ref, rtol=1e-5, atol=1e-5)
+    assert dsa.device_status() == 0
+
+
+def test_decode_ragged_caches(dsa, oracle_mod):
+    """Five sequences in one [B, 4096] cache, filled to different lengths: a full cache, a short
+    one (n < top_k: all keys, -1 padding), exactly top_k and top_k + 1 keys, and an odd length."""
+    wl = W.custom("decode_ragged", B=5, L=1, p0=0, N=4096, top_k=2048, seed=41)
+    run_decode_chain(dsa, oracle_mod, wl, [4096, 100, 2049, 2048, 3001])
+
+
+def test_decode_many_sequences(dsa, oracle_mod):
+    """More sequences than SMs (one split each), top_k not a multiple of the 128-key tile,
+    random cache lengths including 1."""
+    wl = W.custom("decode_many", B=160, L=1, p0=0, N=640, top_k=300, seed=43)
+    rng = np.random.default_rng(44)
+    kv_len = rng.integers(1, wl.N + 1, size=wl.B)
+    kv_len[:3] = [1, wl.N, wl.top_k]
+    run_decode_chain(dsa, oracle_mod, wl, kv_len)
