@@ -3,6 +3,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <cstdint>
+#include <utility>
 
 #include "../../include/dsa.h"
 
@@ -25,6 +26,29 @@ dsa_status_t make_tmap_bf16_2d(CUtensorMap* map, const void* base, uint64_t cols
 // Same with a 64-byte swizzle (box_cols * 2 must be 64).
 dsa_status_t make_tmap_bf16_2d_sw64(CUtensorMap* map, const void* base, uint64_t cols, uint64_t rows,
                                     uint64_t row_bytes, uint32_t box_cols, uint32_t box_rows);
+
+// Launch with programmatic dependent launch allowed: the launch is prepared
+// while the previous kernel on the stream runs and the kernel starts as that
+// kernel's CTAs exit; every kernel of the library runs its prologue (barriers,
+// TMEM allocation) and then waits for its predecessor (griddepcontrol.wait)
+// before it touches global memory.  No kernel triggers its successor early:
+// measured on GB300, successor CTAs waiting next to running ones slowed the
+// batch-8 decode step (36.8 vs 28.7 us as a graph).
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                              Args&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 inline int ceil_div(int a, int b) { return (a + b - 1) / b; }

@@ -112,6 +112,11 @@ __device__ __forceinline__ bool mbar_wait_spin(uint64_t* bar, uint32_t parity, v
     }
 }
 
+// ---------------------------------------------------------------- grid dependencies
+// Wait until the previous kernel on the stream has completed and its memory is
+// visible (returns at once when the launch had no programmatic dependency).
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // ---------------------------------------------------------------- clusters / DSMEM
 __device__ __forceinline__ uint32_t cluster_ctarank() {
     uint32_t r;

@@ -180,6 +180,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
+    griddep_wait();                 // inputs and outputs may belong to the previous kernel until here
 
     if (warp == 0) {
         // ------------------------------------------------------------ TMA producer
@@ -330,7 +331,7 @@ dsa_status_t launch_impl(const void* q_idx, const void* k_idx, const IndexerPara
     auto kern = indexer_kernel<QG, STAGES>;
     if ((st = ensure_smem_attr(reinterpret_cast<const void*>(kern), C::SMEM)) != DSA_OK) return st;
     int grid = min(prm.n_items, device_sm_count());
-    kern<<<grid, kThreads, C::SMEM, stream>>>(tq, tk, prm);
+    if (launch_pdl(kern, dim3(grid), dim3(kThreads), C::SMEM, stream, tq, tk, prm) != cudaSuccess) return DSA_ERR_CUDA;
     return cudaGetLastError() == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
 }
 

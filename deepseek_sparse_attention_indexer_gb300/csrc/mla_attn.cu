@@ -232,6 +232,7 @@ __global__ void __launch_bounds__(kThreads, 1)   // 18 warps: at most 96 registe
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
+    griddep_wait();                 // inputs and outputs may belong to the previous kernel until here
 
     if (warp == 0) {
         // ------------------------------------------------------------ Q loader (TMA)
@@ -612,6 +613,7 @@ __global__ void __launch_bounds__(kThreads, 1)   // 18 warps: at most 96 registe
 // Merge decode partials: out = sum_s exp(lse_s - M) o_s / sum_s exp(lse_s - M).
 __global__ void __launch_bounds__(128) mla_decode_combine_kernel(const float* part_o, const float* part_lse,
                                                                  int nsplit, __nv_bfloat16* out, float* lse) {
+    griddep_wait();
     const int b = blockIdx.x / kH, h = blockIdx.x % kH;
     const float* pl = part_lse + (int64_t)b * nsplit * kH + h;
     float M = -INFINITY;
@@ -645,7 +647,7 @@ dsa_status_t launch_kernel(const void* q, int q_rows, const AttnParams& prm, cud
     auto kern = mla_sparse_attn_kernel<PARTIAL>;
     if ((st = ensure_smem_attr(reinterpret_cast<const void*>(kern), SMEM_BYTES)) != DSA_OK) return st;
     const int grid = min(prm.n_items, device_sm_count());
-    kern<<<grid, kThreads, SMEM_BYTES, stream>>>(tq, prm);
+    if (launch_pdl(kern, dim3(grid), dim3(kThreads), SMEM_BYTES, stream, tq, prm) != cudaSuccess) return DSA_ERR_CUDA;
     return cudaGetLastError() == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
 }
 
@@ -707,8 +709,9 @@ dsa_status_t launch_attn_decode(const void* q, const void* kv, const int32_t* kv
     p.status = device_status_ptr();
     dsa_status_t st = launch_kernel<true>(q, B, p, stream);
     if (st != DSA_OK) return st;
-    mla_decode_combine_kernel<<<B * kH, 128, 0, stream>>>(p.part_o, p.part_lse, p.nsplit,
-                                                         static_cast<__nv_bfloat16*>(out), lse);
+    if (launch_pdl(mla_decode_combine_kernel, dim3(B * kH), dim3(128), 0, stream, (const float*)p.part_o,
+                   (const float*)p.part_lse, p.nsplit, static_cast<__nv_bfloat16*>(out), lse) != cudaSuccess)
+        return DSA_ERR_CUDA;
     return cudaGetLastError() == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
 }
 
@@ -772,8 +775,9 @@ dsa_status_t launch_attn_decode_noalloc(const void* q, const void* kv, const int
     p.status = device_status_ptr();
     st = launch_kernel<true>(q, B, p, stream);
     if (st != DSA_OK) return st;
-    mla_decode_combine_kernel<<<B * kH, 128, 0, stream>>>(p.part_o, p.part_lse, p.nsplit,
-                                                         static_cast<__nv_bfloat16*>(out), lse);
+    if (launch_pdl(mla_decode_combine_kernel, dim3(B * kH), dim3(128), 0, stream, (const float*)p.part_o,
+                   (const float*)p.part_lse, p.nsplit, static_cast<__nv_bfloat16*>(out), lse) != cudaSuccess)
+        return DSA_ERR_CUDA;
     return cudaGetLastError() == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
 }
 

@@ -28,6 +28,7 @@
 #include <cstdint>
 
 #include "dsa_internal.h"
+#include "dsa_ptx.cuh"
 
 namespace dsa {
 
@@ -151,6 +152,7 @@ __global__ void __launch_bounds__(kThreads, 4) topk_stream_kernel(const TopkPara
     __shared__ uint32_t warp_sums[kWarps + 1];
     __shared__ uint32_t sel[3];
 
+    griddep_wait();                 // the scores may still be written by the previous kernel
     const int R = p.B * p.L;
     for (int r = blockIdx.x; r < R; r += gridDim.x) {
         const int b = r / p.L, i = r % p.L;
@@ -248,6 +250,7 @@ __global__ void __launch_bounds__(kThreads, 2) topk_reg_kernel(const TopkParams 
     __shared__ uint32_t warp_sums[kWarps + 1];
     __shared__ uint32_t sel[3];
 
+    griddep_wait();                 // the scores may still be written by the previous kernel
     const int R = p.B * p.L;
     for (int r = blockIdx.x; r < R; r += gridDim.x) {
         const int n = row_keys(p, r);
@@ -332,10 +335,11 @@ dsa_status_t launch_topk(const float* scores, int64_t ld, const int32_t* q_pos0,
     const long long R = (long long)B * L;
     if (Nmax > kRegMinKeys && Nmax <= kChunk) {
         const int grid = (int)min(R, (long long)device_sm_count() * 2);
-        topk_reg_kernel<<<grid, kThreads, 0, stream>>>(p);
+        if (launch_pdl(topk_reg_kernel, dim3(grid), dim3(kThreads), 0, stream, p) != cudaSuccess) return DSA_ERR_CUDA;
     } else {
         const int grid = (int)min(R, (long long)device_sm_count() * 4);
-        topk_stream_kernel<<<grid, kThreads, 0, stream>>>(p);
+        if (launch_pdl(topk_stream_kernel, dim3(grid), dim3(kThreads), 0, stream, p) != cudaSuccess)
+            return DSA_ERR_CUDA;
     }
     return cudaGetLastError() == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
 }
