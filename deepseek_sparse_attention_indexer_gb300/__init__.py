@@ -7,13 +7,16 @@ torch CUDA tensors into device pointers and the current stream.
 
     from deepseek_sparse_attention_indexer_gb300 import indexer_scores, topk, \
         mla_sparse_attn_prefill, mla_sparse_attn_decode
+
+HostPrefill runs a prefill chunk from pinned host buffers with the copies
+overlapped with the kernels (see host_prefill.py).
 """
 
 _API = ("indexer_scores", "topk", "mla_sparse_attn_prefill", "mla_sparse_attn_decode",
         "mla_sparse_attn_decode_noalloc",
         "attn_workspace_size", "device_status", "status_string", "load", "lib_path", "DsaError")
 
-__all__ = list(_API) + ["workloads", "build"]
+__all__ = list(_API) + ["workloads", "build", "HostPrefill"]
 
 
 def __getattr__(name):
@@ -24,4 +27,7 @@ def __getattr__(name):
     if name == "build":
         from ._build import build
         return build
+    if name == "HostPrefill":
+        from .host_prefill import HostPrefill
+        return HostPrefill
     raise AttributeError(name)

@@ -285,3 +285,27 @@ def test_decode_many_sequences(dsa, oracle_mod):
     kv_len = rng.integers(1, wl.N + 1, size=wl.B)
     kv_len[:3] = [1, wl.N, wl.top_k]
     run_decode_chain(dsa, oracle_mod, wl, kv_len)
+
+
+@pytest.mark.parametrize("slices", [1, 3])
+def test_host_prefill_matches_device_calls(dsa, slices):
+    """HostPrefill (pinned host in, pinned host out, copies overlapped) gives the same bits as the
+    three device calls on device copies of the same inputs."""
+    from deepseek_sparse_attention_indexer_gb300.host_prefill import HostPrefill
+    wl = W.custom("host_ragged", B=1, L=77, p0=1100, N=1177, top_k=256, seed=51)
+    qi, ki, w = W.make_indexer_inputs(wl)
+    q, kv = W.make_attention_inputs(wl)
+    q_pos0, kv_len = W.positions(wl)
+    pin = lambda a: torch.from_numpy(np.ascontiguousarray(a.view(np.int16) if a.dtype == np.uint16 else a)).pin_memory()
+    h = [pin(a) for a in (qi, ki, w, q_pos0, kv_len, q, kv)]
+    h_out = torch.empty((wl.L, 64, 512), dtype=torch.bfloat16).pin_memory()
+    runner = HostPrefill(wl.L, wl.N, wl.top_k, slices=slices)
+    for _ in range(2):                  # the buffers are reused across calls
+        runner(*h, h_out, W.SCALE)
+        torch.cuda.synchronize()
+    S = dsa.indexer_scores(dev(qi), dev(ki), dev(w), dev(q_pos0), dev(kv_len))
+    idx = dsa.topk(S, dev(q_pos0), dev(kv_len), wl.N, wl.top_k)
+    ref = dsa.mla_sparse_attn_prefill(dev(q[0]), dev(kv[0]), idx[0], W.SCALE)
+    torch.cuda.synchronize()
+    assert torch.equal(h_out.view(torch.int16), ref.cpu().view(torch.int16))
+    assert dsa.device_status() == 0
