@@ -57,6 +57,30 @@ def algorithmic(wl):
     }
 
 
+def attention_traffic(wl, decode):
+    """DRAM bytes (read + write) of one attention launch at this workload, from the ncu record in
+    profiles/, or None when there is none or the kernel source changed since it was taken."""
+    import hashlib
+    name = "mla_sparse_attn_decode" if decode else "mla_sparse_attn_prefill"
+    src = os.path.join(ROOT, "deepseek_sparse_attention_indexer_gb300", "csrc", "mla_attn.cu")
+    try:
+        sha = hashlib.sha1(open(src, "rb").read()).hexdigest()
+    except OSError:
+        return None
+    pdir = os.path.join(ROOT, "profiles")
+    for fn in sorted(os.listdir(pdir)) if os.path.isdir(pdir) else []:
+        if not (fn.startswith("attention_traffic_") and fn.endswith(".txt")):
+            continue
+        rec = {}
+        for line in open(os.path.join(pdir, fn)):
+            parts = line.split()
+            if len(parts) == 2 and not line.startswith("#"):
+                rec[parts[0]] = parts[1]
+        if rec.get("workload") == wl.name and rec.get("kernel") == name and rec.get("source_sha1") == sha:
+            return int(rec["bytes_per_launch"])
+    return None
+
+
 def load_peaks():
     try:
         with open(PEAKS_PATH) as f:
@@ -307,12 +331,15 @@ def run_gpu(args, wl, rank, world, local_rank):
     if dsa.device_status() != 0:
         raise RuntimeError("device error word set during the graph replays")
 
-    # ---- end to end through the public API with host buffers (pinned), copies timed
+    # ---- end to end through the public API with host buffers (pinned), copies timed.  A decode
+    # step's inputs are the new tokens (indexer query, head weights, absorbed query, positions):
+    # the sequences' key caches (kI, kv) stay resident on the device between steps.
     host_in = [torch.from_numpy(np.ascontiguousarray(a.view(np.int16) if a.dtype == np.uint16 else a)).pin_memory()
                for a in (qi, ki, w, q_pos0, kv_len, q, kv)]
     host_out = torch.empty(tuple(out.shape), dtype=torch.bfloat16).pin_memory()
     dev_in = [h.to(dev) for h in host_in]
-    h2d = sum(h.numel() * h.element_size() for h in host_in)
+    per_step = (0, 2, 3, 4, 5) if decode else range(7)
+    h2d = sum(host_in[i].numel() * host_in[i].element_size() for i in per_step)
     d2h = host_out.numel() * host_out.element_size()
 
     if not decode and wl.B == 1:
@@ -324,11 +351,12 @@ def run_gpu(args, wl, rank, world, local_rank):
         def e2e_step():
             runner(*host_in, host_out, W.SCALE, stream=stream)
     else:
-        e2e_api = "H2D of every input, the calls, D2H of the output, in stream order"
+        e2e_api = ("H2D of the new tokens' inputs (caches resident), the calls, D2H of the output, in stream "
+                   "order" if decode else "H2D of every input, the calls, D2H of the output, in stream order")
 
         def e2e_step():
-            for dv, h in zip(dev_in, host_in):
-                dv.copy_(h, non_blocking=True)
+            for i in per_step:
+                dev_in[i].copy_(host_in[i], non_blocking=True)
             a_qi, a_ki, a_w, a_pos, a_len, a_q, a_kv = dev_in
             dsa.indexer_scores(a_qi, a_ki, a_w, a_pos, a_len, scores=S)
             dsa.topk(S, a_pos, a_len, wl.N, wl.top_k, idx=idx)
@@ -361,13 +389,7 @@ def run_gpu(args, wl, rank, world, local_rank):
     attn_tf = work["attn_flop"] / (kern_ms[2] * 1e-3) / 1e12
     idx_tf = work["indexer_flop"] / (kern_ms[0] * 1e-3) / 1e12
     topk_gbs = work["topk_bytes"] / (kern_ms[1] * 1e-3) / 1e9
-    traffic = None
-    tpath = os.path.join(ROOT, "profiles", "traffic.json")
-    if os.path.exists(tpath):
-        try:
-            traffic = json.load(open(tpath)).get(wl.name, {}).get("mla_sparse_attn")
-        except ValueError:
-            traffic = None
+    traffic = attention_traffic(wl, decode)
     attn_name = "mla_sparse_attn_decode" if decode else "mla_sparse_attn_prefill"
     hbm = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
     gather_gbs = work["gather_bytes"] / (kern_ms[2] * 1e-3) / 1e9
