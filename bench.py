@@ -57,6 +57,25 @@ def algorithmic(wl):
     }
 
 
+def max_over_ranks(x, world, device=None):
+    """The slowest rank's value (the job ends when its last rank does).  One rank: x itself.  The
+    collective runs on the process group's backend (NCCL on the GPU machine, gloo in the CPU tests)."""
+    if world <= 1:
+        return float(x)
+    import torch
+    import torch.distributed as dist
+    on = device if (device is not None and dist.get_backend() == "nccl") else "cpu"
+    t = torch.tensor([float(x)], dtype=torch.float64, device=on)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def replicas_rate(units_per_rank, world, ms):
+    """Whole-job throughput of `world` independent replicas that each process `units_per_rank`
+    in at most `ms` milliseconds (weak scaling: per-rank work fixed as the job grows)."""
+    return units_per_rank * world / (ms * 1e-3)
+
+
 def attention_traffic(wl, decode):
     """DRAM bytes (read + write) of one attention launch at this workload, from the ncu record in
     profiles/, or None when there is none or the kernel source changed since it was taken."""
@@ -293,10 +312,7 @@ def run_gpu(args, wl, rank, world, local_rank):
     per = np.array([[evs[k][i].elapsed_time(evs[k][i + 1]) for i in range(3)] for k in range(args.steps)])
     step_ms = float(per.sum(axis=1).mean())
     kern_ms = per.mean(axis=0)  # indexer, topk, attention
-    t = torch.tensor([step_ms], dtype=torch.float64, device=dev)
-    if world > 1:
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    step_ms_max = float(t.item())
+    step_ms_max = max_over_ranks(step_ms, world, dev)
     status = dsa.device_status()
 
     # ---- the same step replayed as one CUDA graph (launch gaps removed); for
@@ -375,10 +391,7 @@ def run_gpu(args, wl, rank, world, local_rank):
         e1.record(stream)
         torch.cuda.synchronize()
         e2e_ms.append(e0.elapsed_time(e1))
-    t = torch.tensor([float(np.mean(e2e_ms))], dtype=torch.float64, device=dev)
-    if world > 1:
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    e2e_mean = float(t.item())
+    e2e_mean = max_over_ranks(float(np.mean(e2e_ms)), world, dev)
 
     if rank != 0:
         return 0
@@ -403,8 +416,8 @@ def run_gpu(args, wl, rank, world, local_rank):
                 "bytes_per_launch": work["gather_bytes"]}
     else:
         metric = METRIC
-        value, unit, hib = wl.L * wl.B * world / (step_ms_max * 1e-3), UNIT, True
-        e2e_value = wl.L * wl.B * world / (e2e_mean * 1e-3)
+        value, unit, hib = replicas_rate(wl.L * wl.B, world, step_ms_max), UNIT, True
+        e2e_value = replicas_rate(wl.L * wl.B, world, e2e_mean)
         roof = {"bound": "tensor", "kernel": attn_name, "achieved": attn_tf, "peak": peak, "unit": "TFLOP/s",
                 "frac": attn_tf / peak, "traffic": traffic, "peak_kind": f"{peak_kind} bf16 dense burst",
                 "flop_per_launch": work["attn_flop"]}

@@ -309,3 +309,19 @@ def test_host_prefill_matches_device_calls(dsa, slices):
     torch.cuda.synchronize()
     assert torch.equal(h_out.view(torch.int16), ref.cpu().view(torch.int16))
     assert dsa.device_status() == 0
+
+
+def test_chain_128k_keys(dsa, oracle_mod):
+    """Beyond the configs: 16 queries at the end of a 131072-key context (the streaming top-k, 1024
+    key tiles per indexer query group), every output checked."""
+    wl = W.custom("prefill_128k_tail", B=1, L=16, p0=131056, N=131072, top_k=2048, seed=61)
+    (qi, ki, w, q, kv, q_pos0, kv_len), S, idx, out, lse = run_chain(dsa, wl)
+    th = oracle_mod.default_threads()
+    S_ref = oracle_mod.indexer(qi, ki, w, q_pos0, kv_len, threads=th)
+    np.testing.assert_array_equal(S[0, :, : wl.N].cpu().numpy().astype(np.float64), S_ref)
+    idx_ref = oracle_mod.topk(S_ref.astype(np.float32), q_pos0, kv_len, 1, wl.L, wl.top_k, threads=th)
+    np.testing.assert_array_equal(idx[0].cpu().numpy(), idx_ref)
+    o_ref, l_ref = oracle_mod.attention(q[0], kv, idx_ref, np.zeros(wl.L, np.int32), W.SCALE, threads=th)
+    attn_close(out.float().cpu().numpy(), o_ref, wl.name)
+    np.testing.assert_allclose(lse.cpu().numpy(), l_ref, rtol=1e-5, atol=1e-5)
+    assert dsa.device_status() == 0
