@@ -17,13 +17,15 @@
 //     PV reads the very same bytes as the MN-major V^T operand, so the latent
 //     rows are gathered once and used twice (keys and values).
 //   * Sixteen worker warps do both the gather and the softmax.  A worker
-//     warp copies 8 rows of a tile (two per key quarter) with 16-byte
-//     cp.async straight into the swizzled layout.  PV runs one key quarter
-//     at a time and frees each quarter of the stage (its latent rows and
-//     its P^T rows) as soon as it is consumed, so the copies of tile t+1
-//     overlap PV of tile t and only the last quarter's copies sit between
-//     PV(t) and QK(t+1).  The copies of tile t+1 are issued right after the
-//     warp's softmax of tile t, so the whole CTA issues copies (cp.async
+//     warp copies 8 rows of a tile (four per 64-key half) with 16-byte
+//     cp.async straight into the swizzled layout; one warp instruction copies
+//     one 64-dim block of four different rows (8 lanes a row), so the L2
+//     requests in flight spread over many rows rather than long spans of one
+//     (measured: about twice the copy throughput of two-row spans).  PV runs
+//     one key half at a time and frees each half of the stage (its latent
+//     rows and its P^T rows) as soon as it is consumed, so the copies of tile
+//     t+1 overlap PV of tile t.  The copies of tile t+1 are issued right after
+//     the warp's softmax of tile t, so the whole CTA issues copies (cp.async
 //     throughput from L2 grows with the number of issuing warps).  QK waits
 //     per 128-dim chunk of the K-dim.  Unselected or padding slots are
 //     zero-filled.
@@ -64,7 +66,8 @@ constexpr int kWorkerWarps = 16;                  // gather + softmax warps
 constexpr int kWorkers = kWorkerWarps * 32;        // 512
 constexpr int kThreads = 64 + kWorkers;            // warp 0 Q loader, warp 1 MMA, warps 2.. workers
 constexpr int kHG = kH / (kWorkerWarps / 4);       // 16 heads per worker warp
-static_assert(kWorkerWarps == 16 && kTile == 128, "a worker warp copies two rows of each 32-key quarter");
+constexpr int kParts = 2;              // PV releases the stage in two 64-key halves
+static_assert(kWorkerWarps == 16 && kTile == 128, "a worker warp copies four rows of each 64-key half");
 constexpr float kRescaleThreshold = 16.0f;  // log2 units
 
 // smem layout (1024-aligned base)
@@ -75,8 +78,8 @@ constexpr int OFF_MUSED = OFF_RED + 4 * kH * 4;        // float [64]
 constexpr int OFF_ALPHA = OFF_MUSED + kH * 4;          // float [64]
 constexpr int OFF_INVL = OFF_ALPHA + kH * 4;           // float [64]
 constexpr int OFF_BAR = OFF_INVL + kH * 4;
-// barriers: q_full, q_empty, seg_full[5], qtr_free[4], s_full, s_empty, p_full, pv_done
-constexpr int N_BARS = 2 + 5 + 4 + 4;
+// barriers: q_full, q_empty, seg_full[5], part_free[2], s_full, s_empty, p_full, pv_done
+constexpr int N_BARS = 2 + 5 + kParts + 4;
 constexpr int OFF_TMEM = OFF_BAR + N_BARS * 8;
 constexpr int OFF_ABORT = OFF_TMEM + 4;
 constexpr int SMEM_BYTES = OFF_ABORT + 4 + 1024;
@@ -200,11 +203,11 @@ __global__ void __launch_bounds__(kThreads, 1)   // 18 warps: at most 96 registe
     uint64_t* q_full = bars + 0;
     uint64_t* q_empty = bars + 1;
     uint64_t* seg_full = bars + 2;
-    uint64_t* qtr_free = bars + 7;   // key quarter r (rows 32r..32r+31) of the stage consumed by PV
-    uint64_t* s_full = bars + 11;
-    uint64_t* s_empty = bars + 12;
-    uint64_t* p_full = bars + 13;
-    uint64_t* pv_done = bars + 14;
+    uint64_t* part_free = bars + 7;  // key half h (rows 64h..64h+63) of the stage consumed by PV
+    uint64_t* s_full = bars + 7 + kParts;
+    uint64_t* s_empty = s_full + 1;
+    uint64_t* p_full = s_full + 2;
+    uint64_t* pv_done = s_full + 3;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + OFF_TMEM);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + OFF_ABORT);
 
@@ -215,7 +218,7 @@ __global__ void __launch_bounds__(kThreads, 1)   // 18 warps: at most 96 registe
         mbar_init(q_full, 1);
         mbar_init(q_empty, 1);
         for (int c = 0; c < 5; ++c) mbar_init(&seg_full[c], kWorkers);  // one cp.async arrival per worker thread
-        for (int r = 0; r < 4; ++r) mbar_init(&qtr_free[r], 1);
+        for (int h = 0; h < kParts; ++h) mbar_init(&part_free[h], 1);
         mbar_init(s_full, 1);
         mbar_init(s_empty, kWorkerWarps);
         mbar_init(p_full, kWorkerWarps);
@@ -289,17 +292,17 @@ __global__ void __launch_bounds__(kThreads, 1)   // 18 warps: at most 96 registe
                         mma_commit(q_empty);  // the next query's Q^T may stream in during the last softmax
                         q_released = true;
                     }
-                    // ---- O^T += V^T . P^T, 128 latent dims per chunk, one key quarter at a time so
-                    // that the next tile's rows of a quarter stream in as soon as it is consumed
+                    // ---- O^T += V^T . P^T, 128 latent dims per chunk, one key half at a time so
+                    // that the next tile's rows of a half stream in as soon as it is consumed
                     if (!(ok = mbar_wait_spin(p_full, gt & 1, abort_flag, p.status))) break;
                     tc_fence_after();
                     const uint32_t p_base = kv_base + 8 * kBlkBytes;
-                    for (int r = 0; r < 4; ++r) {
+                    for (int r = 0; r < kParts; ++r) {
 #pragma unroll
                         for (int c = 0; c < 4; ++c) {
 #pragma unroll
-                            for (int k2 = 0; k2 < 2; ++k2) {
-                                const int kk = 2 * r + k2;   // 16 keys per K step
+                            for (int k2 = 0; k2 < 8 / kParts; ++k2) {
+                                const int kk = (8 / kParts) * r + k2;   // 16 keys per K step
                                 // A = V^T: MN-major, 64-dim atoms 16 KB apart (LBO), 8-key groups 1 KB apart (SBO)
                                 const uint64_t ad =
                                     sdesc_sw128(kv_base + (2 * c) * kBlkBytes + kk * 2048, kBlkBytes, 1024);
@@ -309,7 +312,7 @@ __global__ void __launch_bounds__(kThreads, 1)   // 18 warps: at most 96 registe
                                             (t > 0 || kk > 0) ? 1u : 0u);
                             }
                         }
-                        mma_commit(&qtr_free[r]);
+                        mma_commit(&part_free[r]);
                     }
                     mma_commit(pv_done);
                 }
@@ -333,11 +336,11 @@ __global__ void __launch_bounds__(kThreads, 1)   // 18 warps: at most 96 registe
 
         // Gather cursor: walks this CTA's (item, tile) sequence one tile ahead
         // of the softmax.  Items without tiles are skipped here.  A worker warp
-        // copies rows 32r + 2ww and 32r + 2ww + 1 of every key quarter r.
+        // copies rows 64h + 4ww .. 64h + 4ww + 3 of each key half h.
         int g_s = 0, g_T = 0, g_t = 0, g_gt = 0;
         Item gI{};
         bool g_valid = false;
-        int g_j = -1;  // lanes 0..7: key of row 32 (lane / 2) + 2 ww + lane % 2 of the cursor's tile
+        int g_j = -1;  // lanes 0..7: key of row 64 (lane / 4) + 4 ww + lane % 4 of the cursor's tile
         auto g_advance_item = [&]() {
             g_valid = false;
             for (;;) {
@@ -359,12 +362,12 @@ __global__ void __launch_bounds__(kThreads, 1)   // 18 warps: at most 96 registe
         auto gather_prep = [&]() {
             g_j = -1;
             if (g_valid && lane < 8) {
-                const int slot = gI.slot0 + g_t * kTile + 32 * (int)(lane >> 1) + 2 * ww + (int)(lane & 1);
+                const int slot = gI.slot0 + g_t * kTile + 64 * (int)(lane >> 2) + 4 * ww + (int)(lane & 3);
                 g_j = (slot < gI.slot_end) ? __ldg(p.idx + (int64_t)gI.row * p.top_k + slot) : -1;
             }
         };
-        // Issue this warp's copies of the cursor's tile, quarter by quarter as PV
-        // frees them, then advance the cursor.  Returns false if a wait gave up.
+        // Issue this warp's copies of the cursor's tile, half by half as PV frees
+        // them, then advance the cursor.  Returns false if a wait gave up.
         auto gather_issue = [&]() -> bool {
             if (!g_valid) return true;
             int j = g_j;
@@ -376,39 +379,25 @@ __global__ void __launch_bounds__(kThreads, 1)   // 18 warps: at most 96 registe
             const uint8_t* src_row = (j >= 0) ? kv_batch + (int64_t)j * kRowBytes : kv_bytes;
             const uint32_t valid_mask = __ballot_sync(0xffffffffu, j >= 0);
             bool ok = true;
-            for (int r = 0; r < 4; ++r) {
-                ok = __all_sync(0xffffffffu, worker_wait(&qtr_free[r], (g_gt & 1) ^ 1, abort_flag, p.status));
+            // One warp instruction copies one 64-dim block (128 B) of four different rows, 8 lanes
+            // per row: requests spread over many rows (and L2 slices) rather than long spans of one.
+            const int i = (int)(lane >> 3);        // which of the warp's 4 rows of the half
+            const int cc = lane & 7;               // 16-byte chunk of the 128-byte block
+            for (int h = 0; h < kParts; ++h) {
+                ok = __all_sync(0xffffffffu, worker_wait(&part_free[h], (g_gt & 1) ^ 1, abort_flag, p.status));
                 if (!ok) break;
-                // latent: 512 dims = 64 chunks of 16 B per row; lanes 0-15 take the first row, 16-31 the second
-                {
-                    const int i = (int)(lane >> 4);
-                    const int row = 32 * r + 2 * ww + i;
-                    const uint8_t* src = reinterpret_cast<const uint8_t*>(
-                        __shfl_sync(0xffffffffu, reinterpret_cast<unsigned long long>(src_row), 2 * r + i));
-                    const uint32_t nbytes = ((valid_mask >> (2 * r + i)) & 1u) ? 16u : 0u;
-                    const int chunk = lane & 15;
-                    const uint32_t row_off = row * 128 + (((chunk & 7) ^ (row & 7)) << 4);
+                const int row = 64 * h + 4 * ww + i;
+                const uint8_t* src = reinterpret_cast<const uint8_t*>(
+                    __shfl_sync(0xffffffffu, reinterpret_cast<unsigned long long>(src_row), 4 * h + i));
+                const uint32_t nbytes = ((valid_mask >> (4 * h + i)) & 1u) ? 16u : 0u;
+                const uint32_t row_off = row * 128 + ((cc ^ (row & 7)) << 4);
 #pragma unroll
-                    for (int c = 0; c < 4; ++c) {
-                        const int blk = 2 * c + (chunk >> 3);
-                        cp_async_16(kv_smem + blk * kBlkBytes + row_off, src + (c * 16 + chunk) * 16, nbytes);
-                        if (r == 3) cp_async_arrive_noinc(&seg_full[c]);
-                    }
+                for (int blk = 0; blk < 9; ++blk) {
+                    cp_async_16(kv_smem + blk * kBlkBytes + row_off, src + blk * 128 + cc * 16, nbytes);
+                    // the last half completes latent chunk c with block 2c+1, the rope with block 8
+                    if (h == kParts - 1 && (blk & 1) == 1) cp_async_arrive_noinc(&seg_full[blk >> 1]);
                 }
-                // rope: 64 dims = 8 chunks per row; lanes 0-7 the first row, 8-15 the second
-                {
-                    const int i = (int)((lane >> 3) & 1u);
-                    const int row = 32 * r + 2 * ww + i;
-                    const uint8_t* src = reinterpret_cast<const uint8_t*>(
-                        __shfl_sync(0xffffffffu, reinterpret_cast<unsigned long long>(src_row), 2 * r + i));
-                    if (lane < 16) {
-                        const uint32_t nbytes = ((valid_mask >> (2 * r + i)) & 1u) ? 16u : 0u;
-                        const int cc = lane & 7;
-                        cp_async_16(kv_smem + 8 * kBlkBytes + row * 128 + ((cc ^ (row & 7)) << 4),
-                                    src + (64 + cc) * 16, nbytes);
-                    }
-                    if (r == 3) cp_async_arrive_noinc(&seg_full[4]);
-                }
+                if (h == kParts - 1) cp_async_arrive_noinc(&seg_full[4]);
             }
             ++g_gt;
             if (++g_t >= g_T) g_advance_item();
