@@ -75,7 +75,8 @@ def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
                 print(out)
     if force or jobs or _stale(LIB_PATH, objs):
         tmp = LIB_PATH + ".tmp%d" % os.getpid()
-        run([nvcc, *ARCH_FLAGS, "-shared", "-o", tmp, *objs])
+        # every symbol must resolve at link time: a missing definition fails the build, not a later load
+        run([nvcc, *ARCH_FLAGS, "-shared", "-Xlinker", "--no-undefined", "-o", tmp, *objs])
         os.replace(tmp, LIB_PATH)
     return LIB_PATH
 

@@ -112,10 +112,6 @@ dsa_status_t make_tmap_bf16_2d(CUtensorMap* map, const void* base, uint64_t cols
                                uint32_t box_cols, uint32_t box_rows) {
     return make_tmap_impl(map, base, cols, rows, row_bytes, box_cols, box_rows, CU_TENSOR_MAP_SWIZZLE_128B);
 }
-dsa_status_t make_tmap_bf16_2d_sw64(CUtensorMap* map, const void* base, uint64_t cols, uint64_t rows,
-                                    uint64_t row_bytes, uint32_t box_cols, uint32_t box_rows) {
-    return make_tmap_impl(map, base, cols, rows, row_bytes, box_cols, box_rows, CU_TENSOR_MAP_SWIZZLE_64B);
-}
 
 }  // namespace dsa
 

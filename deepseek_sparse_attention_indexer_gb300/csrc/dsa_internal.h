@@ -23,9 +23,6 @@ dsa_status_t ensure_smem_attr(const void* func, int bytes);
 // box = box_cols x box_rows, 128-byte swizzle, zero fill out of bounds.
 dsa_status_t make_tmap_bf16_2d(CUtensorMap* map, const void* base, uint64_t cols, uint64_t rows,
                                uint64_t row_bytes, uint32_t box_cols, uint32_t box_rows);
-// Same with a 64-byte swizzle (box_cols * 2 must be 64).
-dsa_status_t make_tmap_bf16_2d_sw64(CUtensorMap* map, const void* base, uint64_t cols, uint64_t rows,
-                                    uint64_t row_bytes, uint32_t box_cols, uint32_t box_rows);
 
 // Launch with programmatic dependent launch allowed: the launch is prepared
 // while the previous kernel on the stream runs and the kernel starts as that
