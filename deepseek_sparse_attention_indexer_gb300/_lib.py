@@ -40,6 +40,9 @@ SIGNATURES = {
     "mla_sparse_attn_workspace_size": (_SZ, [_I, _I, _I, _I]),
     "mla_sparse_attn_decode": (ctypes.c_int32, [_P, _P, _P, _P, _I, _I, _I, _F, _P, _P, _P, _SZ, _P]),
     "mla_sparse_attn_decode_noalloc": (ctypes.c_int32, [_P, _P, _P, _P, _I, _I, _I, _F, _P, _P, _P]),
+    "dsa_indexer_scores_paged": (ctypes.c_int32, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _I64, _P]),
+    "mla_sparse_attn_decode_paged": (ctypes.c_int32, [_P, _P, _P, _P, _I, _I, _I, _P, _I, _I, _I, _F, _P, _P, _P,
+                                                      _SZ, _P]),
     "dsa_device_status": (ctypes.c_int32, [_P, ctypes.POINTER(ctypes.c_int32), _I]),
 }
 
@@ -194,6 +197,50 @@ def mla_sparse_attn_decode_noalloc(q: torch.Tensor, kv: torch.Tensor, kv_len: to
     rc = load().mla_sparse_attn_decode_noalloc(_ptr(q), _ptr(kv), _ptr(kv_len), _ptr(idx), B, Nmax, top_k,
                                                float(scale), _ptr(out), _ptr(lse), _stream(stream))
     _check("mla_sparse_attn_decode_noalloc", rc)
+    return (out, lse) if want_lse else out
+
+
+def indexer_scores_paged(q_idx: torch.Tensor, k_pool: torch.Tensor, w: torch.Tensor, q_pos0: torch.Tensor,
+                         kv_len: torch.Tensor, block_table: torch.Tensor, page_size: int, Nmax: int,
+                         scores: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """indexer_scores over a paged key cache: k_pool [num_pages * page_size, 128] bf16,
+    block_table [B, bt_stride] int32 (pool page of each logical page of a sequence)."""
+    B, L, Hi, Di = q_idx.shape
+    assert _is16(q_idx) and _is16(k_pool) and w.dtype == torch.float32 and block_table.dtype == torch.int32
+    num_pages = k_pool.shape[0] // page_size
+    if scores is None:
+        ld = (Nmax + 3) // 4 * 4
+        scores = torch.empty((B, L, ld), dtype=torch.float32, device=q_idx.device)
+    ld = scores.shape[-1]
+    rc = load().dsa_indexer_scores_paged(_ptr(q_idx), _ptr(k_pool), _ptr(w), _ptr(q_pos0), _ptr(kv_len),
+                                         _ptr(block_table), block_table.shape[1], page_size, num_pages,
+                                         B, L, Nmax, _ptr(scores), ld, _stream(stream))
+    _check("dsa_indexer_scores_paged", rc)
+    return scores
+
+
+def mla_sparse_attn_decode_paged(q: torch.Tensor, kv_pool: torch.Tensor, kv_len: torch.Tensor,
+                                 block_table: torch.Tensor, page_size: int, idx: torch.Tensor, scale: float,
+                                 Nmax: int, out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
+                                 workspace: Optional[torch.Tensor] = None, want_lse: bool = False, stream=None):
+    """mla_sparse_attn_decode over a paged cache: kv_pool [num_pages * page_size, 576] bf16,
+    block_table [B, bt_stride] int32; idx holds logical key positions."""
+    B = q.shape[0]
+    top_k = idx.shape[-1]
+    assert _is16(q) and _is16(kv_pool) and idx.dtype == torch.int32 and block_table.dtype == torch.int32
+    num_pages = kv_pool.shape[0] // page_size
+    if out is None:
+        out = torch.empty((B, 64, 512), dtype=torch.bfloat16, device=q.device)
+    if lse is None and want_lse:
+        lse = torch.empty((B, 64), dtype=torch.float32, device=q.device)
+    ws_bytes = attn_workspace_size(B, top_k)
+    if workspace is None:
+        workspace = torch.empty((ws_bytes,), dtype=torch.uint8, device=q.device)
+    rc = load().mla_sparse_attn_decode_paged(_ptr(q), _ptr(kv_pool), _ptr(kv_len), _ptr(block_table),
+                                             block_table.shape[1], page_size, num_pages, _ptr(idx), B, Nmax,
+                                             top_k, float(scale), _ptr(out), _ptr(lse), _ptr(workspace),
+                                             workspace.numel(), _stream(stream))
+    _check("mla_sparse_attn_decode_paged", rc)
     return (out, lse) if want_lse else out
 
 

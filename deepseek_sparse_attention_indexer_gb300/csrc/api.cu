@@ -149,7 +149,41 @@ dsa_status_t dsa_indexer_scores(const void* q_idx, const void* k_idx, const floa
         return DSA_ERR_MISALIGNED;
     dsa_status_t st = check_device();
     if (st != DSA_OK) return st;
-    return launch_indexer(q_idx, k_idx, w, q_pos0, kv_len, B, L, Nmax, scores, ld,
+    return launch_indexer(q_idx, k_idx, w, q_pos0, kv_len, B, L, Nmax, scores, ld, PageTable{},
+                          static_cast<cudaStream_t>(stream));
+}
+
+namespace {
+// Host checks of a page table's geometry; fills `pt` on success.
+dsa_status_t make_page_table(const int32_t* table, int stride, int page_size, int num_pages, int Nmax,
+                             PageTable* pt) {
+    if (!table) return DSA_ERR_INVALID_ARG;
+    if (stride < 1 || num_pages < 1) return DSA_ERR_INVALID_ARG;
+    if (page_size < 16 || page_size > 65536 || (page_size & (page_size - 1)) != 0) return DSA_ERR_UNSUPPORTED_SHAPE;
+    if ((long long)num_pages * page_size > 0x7FFFFFFFLL) return DSA_ERR_UNSUPPORTED_SHAPE;
+    if ((long long)stride * page_size < Nmax) return DSA_ERR_INVALID_ARG;
+    int shift = 0;
+    while ((1 << shift) < page_size) ++shift;
+    *pt = PageTable{table, stride, shift, num_pages};
+    return DSA_OK;
+}
+}  // namespace
+
+dsa_status_t dsa_indexer_scores_paged(const void* q_idx, const void* k_pool, const float* w, const int32_t* q_pos0,
+                                      const int32_t* kv_len, const int32_t* block_table, int bt_stride,
+                                      int page_size, int num_pages, int B, int L, int Nmax, float* scores,
+                                      int64_t ld, void* stream) {
+    if (!q_idx || !k_pool || !w || !q_pos0 || !kv_len || !scores) return DSA_ERR_INVALID_ARG;
+    if (B < 1 || L < 1 || Nmax < 1 || ld < Nmax) return DSA_ERR_INVALID_ARG;
+    if ((long long)B * L * DSA_INDEXER_HEADS > 0x7FFFFFFFLL) return DSA_ERR_UNSUPPORTED_SHAPE;
+    PageTable pt;
+    dsa_status_t st = make_page_table(block_table, bt_stride, page_size, num_pages, Nmax, &pt);
+    if (st != DSA_OK) return st;
+    if ((long long)B * bt_stride > 0x7FFFFFFFLL) return DSA_ERR_UNSUPPORTED_SHAPE;
+    if (!aligned16(q_idx) || !aligned16(k_pool) || !aligned16(w) || !aligned16(scores) || (ld % 4) != 0)
+        return DSA_ERR_MISALIGNED;
+    if ((st = check_device()) != DSA_OK) return st;
+    return launch_indexer(q_idx, k_pool, w, q_pos0, kv_len, B, L, Nmax, scores, ld, pt,
                           static_cast<cudaStream_t>(stream));
 }
 
@@ -208,7 +242,26 @@ dsa_status_t mla_sparse_attn_decode(const void* q, const void* kv, const int32_t
     if (ws_bytes < attn_decode_workspace(B, top_k)) return DSA_ERR_WORKSPACE_TOO_SMALL;
     dsa_status_t st = check_device();
     if (st != DSA_OK) return st;
-    return launch_attn_decode(q, kv, kv_len, idx, B, Nmax, top_k, scale, out, lse, workspace,
+    return launch_attn_decode(q, kv, kv_len, idx, B, Nmax, top_k, scale, out, lse, workspace, PageTable{},
+                              static_cast<cudaStream_t>(stream));
+}
+
+dsa_status_t mla_sparse_attn_decode_paged(const void* q, const void* kv_pool, const int32_t* kv_len,
+                                          const int32_t* block_table, int bt_stride, int page_size, int num_pages,
+                                          const int32_t* idx, int B, int Nmax, int top_k, float scale, void* out,
+                                          float* lse, void* workspace, size_t ws_bytes, void* stream) {
+    if (!q || !kv_pool || !kv_len || !idx || !out || !workspace) return DSA_ERR_INVALID_ARG;
+    if (B < 1 || Nmax < 1) return DSA_ERR_INVALID_ARG;
+    if (top_k < 1 || top_k > DSA_MAX_TOPK) return DSA_ERR_UNSUPPORTED_SHAPE;
+    if (!(scale > 0.f) || !(scale < 1e30f)) return DSA_ERR_INVALID_ARG;
+    PageTable pt;
+    dsa_status_t st = make_page_table(block_table, bt_stride, page_size, num_pages, Nmax, &pt);
+    if (st != DSA_OK) return st;
+    if ((long long)B * bt_stride > 0x7FFFFFFFLL) return DSA_ERR_UNSUPPORTED_SHAPE;
+    if (!aligned16(q) || !aligned16(kv_pool) || !aligned16(out) || !aligned16(workspace)) return DSA_ERR_MISALIGNED;
+    if (ws_bytes < attn_decode_workspace(B, top_k)) return DSA_ERR_WORKSPACE_TOO_SMALL;
+    if ((st = check_device()) != DSA_OK) return st;
+    return launch_attn_decode(q, kv_pool, kv_len, idx, B, Nmax, top_k, scale, out, lse, workspace, pt,
                               static_cast<cudaStream_t>(stream));
 }
 

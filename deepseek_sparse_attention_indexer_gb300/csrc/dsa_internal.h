@@ -48,12 +48,23 @@ inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, s
 }
 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Page table of a paged key cache: logical key j of sequence b is pool row
+// table[b * stride + (j >> shift)] * 2^shift + (j & (2^shift - 1)).  A null
+// table means the dense layout, row b * Nmax + j.
+struct PageTable {
+    const int32_t* table;
+    int stride;      // entries per sequence
+    int shift;       // log2(page_size)
+    int num_pages;   // pages in the pool
+};
+
 inline int ceil_div(int a, int b) { return (a + b - 1) / b; }
 
 // Launch entry points implemented in the kernel files.
 dsa_status_t launch_indexer(const void* q_idx, const void* k_idx, const float* w, const int32_t* q_pos0,
                             const int32_t* kv_len, int B, int L, int Nmax, float* scores, int64_t ld,
-                            cudaStream_t stream);
+                            const PageTable& pages, cudaStream_t stream);
 dsa_status_t launch_topk(const float* scores, int64_t ld, const int32_t* q_pos0, const int32_t* kv_len, int B,
                          int L, int Nmax, int top_k, int32_t* idx, cudaStream_t stream);
 dsa_status_t launch_attn_prefill(const void* q, const void* kv, const int32_t* idx, int L, int N, int top_k,
@@ -64,6 +75,6 @@ dsa_status_t launch_attn_decode_noalloc(const void* q, const void* kv, const int
                                         cudaStream_t stream);
 dsa_status_t launch_attn_decode(const void* q, const void* kv, const int32_t* kv_len, const int32_t* idx, int B,
                                 int Nmax, int top_k, float scale, void* out, float* lse, void* workspace,
-                                cudaStream_t stream);
+                                const PageTable& pages, cudaStream_t stream);
 
 }  // namespace dsa

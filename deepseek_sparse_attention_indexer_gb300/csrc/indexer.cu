@@ -61,6 +61,8 @@ struct IndexerParams {
     int CH;       // key tiles per chunk
     int n_items;  // B * G * NC
     int32_t* status;  // device error word
+    PageTable pages;  // paged key cache (pages.table == nullptr: dense [B][Nmax] rows)
+    int box_rows;     // rows per key TMA box: 128 dense, min(page_size, 128) paged
 };
 
 template <int QG, int STAGES>
@@ -203,10 +205,32 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const int st = it % STAGES;
                     if (!(ok = mbar_wait_spin(&a_empty[st], ((it / STAGES) & 1) ^ 1, abort_flag, p.status))) break;
                     mbar_arrive_expect_tx(&a_full[st], C::A_BYTES);
-                    const int krow = I.b * p.Nmax + t * kTileKeys;
                     uint8_t* dst = sA + st * C::A_BYTES;
-                    tma_load_2d(dst, &tmap_k, &a_full[st], 0, krow);
-                    tma_load_2d(dst + C::A_HALF, &tmap_k, &a_full[st], 64, krow);
+                    if (p.pages.table == nullptr) {
+                        const int krow = I.b * p.Nmax + t * kTileKeys;
+                        tma_load_2d(dst, &tmap_k, &a_full[st], 0, krow);
+                        tma_load_2d(dst + C::A_HALF, &tmap_k, &a_full[st], 64, krow);
+                    } else {
+                        // one box per page (or per 128 rows of a larger page); a box
+                        // starts on a 1024-byte boundary, so the swizzled rows land
+                        // exactly where one 128-row box would put them
+                        for (int r = 0; r < kTileKeys; r += p.box_rows) {
+                            const int j = t * kTileKeys + r;   // logical key of the box's first row
+                            const int lp = j >> p.pages.shift;
+                            int page = 0;
+                            if (j < I.kl) {
+                                page = __ldg(p.pages.table + (int64_t)I.b * p.pages.stride + lp);
+                                if (page < 0 || page >= p.pages.num_pages) {
+                                    raise_dev_error(p.status, DEV_ERR_BOUNDS);
+                                    page = -1;   // a box wholly outside the pool: TMA fills zeros
+                                }
+                            }
+                            const int krow = (page < 0) ? -p.box_rows
+                                                        : (page << p.pages.shift) + (j & ((1 << p.pages.shift) - 1));
+                            tma_load_2d(dst + r * 128, &tmap_k, &a_full[st], 0, krow);
+                            tma_load_2d(dst + C::A_HALF + r * 128, &tmap_k, &a_full[st], 64, krow);
+                        }
+                    }
                 }
             }
         }
@@ -327,7 +351,8 @@ dsa_status_t launch_impl(const void* q_idx, const void* k_idx, const IndexerPara
     CUtensorMap tq, tk;
     dsa_status_t st;
     if ((st = make_tmap_bf16_2d(&tq, q_idx, kDi, (uint64_t)B * L * kHi, kDi * 2, 64, QG * kHi)) != DSA_OK) return st;
-    if ((st = make_tmap_bf16_2d(&tk, k_idx, kDi, (uint64_t)B * Nmax, kDi * 2, 64, kTileKeys)) != DSA_OK) return st;
+    const uint64_t k_rows = prm.pages.table ? ((uint64_t)prm.pages.num_pages << prm.pages.shift) : (uint64_t)B * Nmax;
+    if ((st = make_tmap_bf16_2d(&tk, k_idx, kDi, k_rows, kDi * 2, 64, prm.box_rows)) != DSA_OK) return st;
     auto kern = indexer_kernel<QG, STAGES>;
     if ((st = ensure_smem_attr(reinterpret_cast<const void*>(kern), C::SMEM)) != DSA_OK) return st;
     int grid = min(prm.n_items, device_sm_count());
@@ -339,7 +364,7 @@ dsa_status_t launch_impl(const void* q_idx, const void* k_idx, const IndexerPara
 
 dsa_status_t launch_indexer(const void* q_idx, const void* k_idx, const float* w, const int32_t* q_pos0,
                             const int32_t* kv_len, int B, int L, int Nmax, float* scores, int64_t ld,
-                            cudaStream_t stream) {
+                            const PageTable& pages, cudaStream_t stream) {
     const int QG = (L == 1) ? 1 : 8;
     IndexerParams p;
     p.w = w;
@@ -365,6 +390,8 @@ dsa_status_t launch_indexer(const void* q_idx, const void* k_idx, const float* w
     if (items > 0x7FFFFFFFLL) return DSA_ERR_UNSUPPORTED_SHAPE;
     p.n_items = (int)items;
     p.status = device_status_ptr();
+    p.pages = pages;
+    p.box_rows = pages.table ? (pages.shift >= 7 ? kTileKeys : (1 << pages.shift)) : kTileKeys;
     if (QG == 8) return launch_impl<8, 4>(q_idx, k_idx, p, B, L, Nmax, stream);
     return launch_impl<1, 4>(q_idx, k_idx, p, B, L, Nmax, stream);
 }

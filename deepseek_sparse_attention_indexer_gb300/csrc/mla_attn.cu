@@ -107,6 +107,7 @@ struct AttnParams {
     int n_items;               // rows * nsplit
     float scale_log2;          // scale * log2(e)
     int32_t* status;           // device error word
+    PageTable pages;           // paged cache (pages.table == nullptr: dense rows)
 };
 
 // Waits of the worker warps (every lane polls).
@@ -375,8 +376,17 @@ __global__ void __launch_bounds__(kThreads, 1)   // 18 warps: at most 96 registe
                 raise_dev_error(p.status, DEV_ERR_BOUNDS);
                 j = -1;
             }
-            const uint8_t* kv_batch = kv_bytes + (int64_t)gI.batch * p.Nmax * kRowBytes;
-            const uint8_t* src_row = (j >= 0) ? kv_batch + (int64_t)j * kRowBytes : kv_bytes;
+            int64_t prow = (int64_t)gI.batch * p.Nmax + j;   // cache row of key j
+            if (PARTIAL && j >= 0 && p.pages.table != nullptr) {   // paged caches: decode only
+                const int page = __ldg(p.pages.table + (int64_t)gI.batch * p.pages.stride + (j >> p.pages.shift));
+                if (page < 0 || page >= p.pages.num_pages) {
+                    raise_dev_error(p.status, DEV_ERR_BOUNDS);
+                    j = -1;
+                } else {
+                    prow = ((int64_t)page << p.pages.shift) + (j & ((1 << p.pages.shift) - 1));
+                }
+            }
+            const uint8_t* src_row = (j >= 0) ? kv_bytes + prow * kRowBytes : kv_bytes;
             const uint32_t valid_mask = __ballot_sync(0xffffffffu, j >= 0);
             bool ok = true;
             // One warp instruction copies one 64-dim block (128 B) of four different rows, 8 lanes
@@ -600,24 +610,35 @@ __global__ void __launch_bounds__(kThreads, 1)   // 18 warps: at most 96 registe
 }
 
 // Merge decode partials: out = sum_s exp(lse_s - M) o_s / sum_s exp(lse_s - M).
+// A sequence has at most kMaxSplits splits (top_k <= DSA_MAX_TOPK, at least 128
+// slots per split); every thread issues all of its split loads before using any.
+constexpr int kMaxSplits = DSA_MAX_TOPK / kTile;
 __global__ void __launch_bounds__(128) mla_decode_combine_kernel(const float* part_o, const float* part_lse,
                                                                  int nsplit, __nv_bfloat16* out, float* lse) {
     griddep_wait();
     const int b = blockIdx.x / kH, h = blockIdx.x % kH;
     const float* pl = part_lse + (int64_t)b * nsplit * kH + h;
+    float ls[kMaxSplits];
+    float4 v[kMaxSplits];
+#pragma unroll
+    for (int s = 0; s < kMaxSplits; ++s) {
+        ls[s] = (s < nsplit) ? pl[(int64_t)s * kH] : -INFINITY;
+        v[s] = (s < nsplit) ? reinterpret_cast<const float4*>(part_o + (((int64_t)b * nsplit + s) * kH + h) * kDv)[threadIdx.x]
+                            : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
     float M = -INFINITY;
-    for (int s = 0; s < nsplit; ++s) M = fmaxf(M, pl[(int64_t)s * kH]);
+#pragma unroll
+    for (int s = 0; s < kMaxSplits; ++s) M = fmaxf(M, ls[s]);
     float wsum = 0.f;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int s = 0; s < nsplit; ++s) {
-        const float ls = pl[(int64_t)s * kH];
-        const float wgt = (M == -INFINITY) ? 0.f : expf(ls - M);
+#pragma unroll
+    for (int s = 0; s < kMaxSplits; ++s) {
+        const float wgt = (M == -INFINITY || ls[s] == -INFINITY) ? 0.f : expf(ls[s] - M);
         wsum += wgt;
-        const float4 v = reinterpret_cast<const float4*>(part_o + (((int64_t)b * nsplit + s) * kH + h) * kDv)[threadIdx.x];
-        acc.x += wgt * v.x;
-        acc.y += wgt * v.y;
-        acc.z += wgt * v.z;
-        acc.w += wgt * v.w;
+        acc.x += wgt * v[s].x;
+        acc.y += wgt * v[s].y;
+        acc.z += wgt * v[s].z;
+        acc.w += wgt * v[s].w;
     }
     const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
     __nv_bfloat16* dst = out + ((int64_t)b * kH + h) * kDv + 4 * threadIdx.x;
@@ -677,7 +698,7 @@ size_t attn_decode_workspace(int B, int top_k) {
 
 dsa_status_t launch_attn_decode(const void* q, const void* kv, const int32_t* kv_len, const int32_t* idx, int B,
                                 int Nmax, int top_k, float scale, void* out, float* lse, void* workspace,
-                                cudaStream_t stream) {
+                                const PageTable& pages, cudaStream_t stream) {
     const int ns = decode_splits(B, top_k);
     const int tiles = ceil_div(top_k, kTile);
     AttnParams p{};
@@ -696,6 +717,7 @@ dsa_status_t launch_attn_decode(const void* q, const void* kv, const int32_t* kv
     p.n_items = B * p.nsplit;
     p.scale_log2 = scale * 1.4426950408889634f;
     p.status = device_status_ptr();
+    p.pages = pages;
     dsa_status_t st = launch_kernel<true>(q, B, p, stream);
     if (st != DSA_OK) return st;
     if (launch_pdl(mla_decode_combine_kernel, dim3(B * kH), dim3(128), 0, stream, (const float*)p.part_o,

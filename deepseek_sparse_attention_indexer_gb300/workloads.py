@@ -164,3 +164,36 @@ def random_scores(rows: int, n: int, seed: int, ties: bool = True) -> np.ndarray
         big = rng.random((rows, n)) < 0.01
         s[big] *= np.float32(1e30)
     return s
+
+
+def paginate(dense: np.ndarray, kv_len, page_size: int, extra_pages: int = 0, seed: int = 0):
+    """Lay dense per-sequence cache rows [B, Nmax, D] out as a paged pool.
+
+    Every page that holds a key j < kv_len[b] goes to a distinct, seeded-random
+    page of the pool; `extra_pages` more pages (never referenced) and the tail
+    rows of each sequence's last page hold seeded junk, so a wrong page lookup
+    changes the result.  Table entries of pages past kv_len[b] are -1.
+    Returns (pool [num_pages * page_size, D], block_table int32 [B, ceil(Nmax / page_size)]).
+    """
+    B, Nmax, D = dense.shape
+    kv_len = np.asarray(kv_len, np.int64)
+    stride = -(-Nmax // page_size)
+    used = [int(-(-int(n) // page_size)) for n in kv_len]
+    num_pages = sum(used) + extra_pages
+    rng = np.random.default_rng(seed)
+    perm = rng.permutation(num_pages)
+    if dense.dtype == np.uint16:
+        pool = f32_to_bf16_bits(rng.standard_normal((num_pages * page_size, D), dtype=np.float32))
+    else:
+        pool = rng.standard_normal((num_pages * page_size, D)).astype(dense.dtype)
+    table = np.full((B, stride), -1, np.int32)
+    k = 0
+    for b in range(B):
+        for lp in range(used[b]):
+            page = int(perm[k])
+            k += 1
+            table[b, lp] = page
+            lo = lp * page_size
+            hi = min(lo + page_size, int(kv_len[b]))
+            pool[page * page_size: page * page_size + hi - lo] = dense[b, lo:hi]
+    return pool, table

@@ -33,7 +33,7 @@
 extern "C" {
 #endif
 
-#define DSA_ABI_VERSION 1
+#define DSA_ABI_VERSION 2  /* 2: paged-cache entry points */
 
 #define DSA_INDEXER_HEADS 32
 #define DSA_INDEXER_DIM 128
@@ -185,6 +185,45 @@ dsa_status_t mla_sparse_attn_decode(const void *q, const void *kv, const int32_t
 dsa_status_t mla_sparse_attn_decode_noalloc(const void *q, const void *kv, const int32_t *kv_len,
                                             const int32_t *idx, int B, int Nmax, int top_k,
                                             float scale, void *out, float *lse, void *stream);
+
+/*
+ * Paged caches.  Serving engines keep each sequence's cache rows in fixed-size
+ * pages of one shared pool instead of a dense [B, Nmax, ...] block (exo PR
+ * #2539 batches decode through per-sequence "batch caches", section "Decode";
+ * the page table is this library's layout for them).  The two calls below read
+ * the keys through a page table; everything else (positions, kv_len, the
+ * top-k, the results) is exactly as in dsa_indexer_scores and
+ * mla_sparse_attn_decode with the dense cache
+ *
+ *   k[b, j, :] = pool[block_table[b * bt_stride + j / page_size] * page_size + j % page_size, :]
+ *
+ * for every key j < kv_len[b].  So dsa_topk runs unchanged on the scores and
+ * the selected indices stay logical key positions.
+ *
+ *   block_table  int32 [B, bt_stride] (device): pool page of each logical page.
+ *                Entries of pages that hold a key j < kv_len[b] must lie in
+ *                [0, num_pages); an entry outside that range is recorded as
+ *                DSA_ERR_DEVICE_BOUNDS and its rows are read as zeros.  Entries
+ *                of later pages are never read.
+ *   page_size    rows per page: a power of two, 16 <= page_size <= 65536.
+ *   num_pages    pages in the pool; num_pages * page_size <= 2^31 - 1.
+ *   Nmax         the largest kv_len (a bound, as for the dense calls);
+ *                Nmax <= bt_stride * page_size.
+ *   k_pool       bf16 [num_pages * page_size, 128]   indexer keys
+ *   kv_pool      bf16 [num_pages * page_size, 576]   latent cache rows
+ * Any L works for the indexer (chunked prefill over a paged cache as well as
+ * decode); the attention call is the decode one (one query per sequence).
+ */
+dsa_status_t dsa_indexer_scores_paged(const void *q_idx, const void *k_pool, const float *w,
+                                      const int32_t *q_pos0, const int32_t *kv_len,
+                                      const int32_t *block_table, int bt_stride, int page_size,
+                                      int num_pages, int B, int L, int Nmax, float *scores,
+                                      int64_t ld, void *stream);
+dsa_status_t mla_sparse_attn_decode_paged(const void *q, const void *kv_pool, const int32_t *kv_len,
+                                          const int32_t *block_table, int bt_stride, int page_size,
+                                          int num_pages, const int32_t *idx, int B, int Nmax,
+                                          int top_k, float scale, void *out, float *lse,
+                                          void *workspace, size_t ws_bytes, void *stream);
 
 /*
  * dsa_device_status -- synchronise `stream`, then read (and if `reset` is

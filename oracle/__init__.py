@@ -164,3 +164,27 @@ def attention(q: np.ndarray, kv: np.ndarray, idx: np.ndarray, row_batch: np.ndar
                         Dv, float(scale), b, e, _ptr(out) + k * H * Dv * 8, _ptr(lse) + k * H * 8)
     _run(fn, _split(rows, threads), threads)
     return out, lse
+
+
+def unpage(pool: np.ndarray, block_table: np.ndarray, page_size: int, kv_len,
+           Nmax: int) -> np.ndarray:
+    """Dense [B, Nmax, D] cache of a paged one, by the page-table definition.
+
+    Row j < kv_len[b] of sequence b is pool row
+    block_table[b, j // page_size] * page_size + j % page_size.  A table entry
+    outside [0, num_pages) reads as a zero row (the library's stated reading of
+    a bad entry), and rows j >= kv_len[b] are zero: nothing downstream reads
+    them.  Paging only moves rows; no arithmetic happens here.  The pages
+    describe exo's per-sequence decode "batch caches" (exo PR #2539, section
+    "Decode") without fixing a memory layout; the page table is the library's.
+    """
+    B = block_table.shape[0]
+    D = pool.shape[1]
+    num_pages = pool.shape[0] // page_size
+    out = np.zeros((B, Nmax, D), dtype=pool.dtype)
+    for b in range(B):
+        for j in range(int(kv_len[b])):
+            page = int(block_table[b, j // page_size])
+            if 0 <= page < num_pages:
+                out[b, j] = pool[page * page_size + j % page_size]
+    return out

@@ -31,7 +31,7 @@ def test_header_declares_the_path():
     names = declared_functions()
     for n in ["dsa_indexer_scores", "dsa_topk", "mla_sparse_attn_prefill", "mla_sparse_attn_decode",
               "dsa_status_string", "dsa_abi_version", "dsa_device_status", "dsa_topk_workspace_size",
-              "mla_sparse_attn_workspace_size"]:
+              "mla_sparse_attn_workspace_size", "dsa_indexer_scores_paged", "mla_sparse_attn_decode_paged"]:
         assert n in names
 
 
@@ -47,7 +47,7 @@ def test_exports_every_declared_symbol(lib):
 
 
 def test_version_and_strings(lib):
-    assert lib.dsa_abi_version() == 1
+    assert lib.dsa_abi_version() == 2
     for code in range(0, 10):
         s = lib.dsa_status_string(code)
         assert s and len(s) > 1
@@ -77,6 +77,19 @@ def test_host_validation_rejects_bad_arguments(lib):
     assert ws > 0 and lib.mla_sparse_attn_workspace_size(1, 4096, 2048, 0) == 0
     assert lib.mla_sparse_attn_decode(P, P, P, P, 8, 4096, 2048, 0.0625, P, None, P, ws - 1, stream) == 4
     assert lib.mla_sparse_attn_decode(P, P, P, P, 8, 4096, 2048, 0.0625, P, None, None, ws, stream) == 1
+    # paged caches: (block_table, bt_stride, page_size, num_pages) geometry
+    idx_paged = lib.dsa_indexer_scores_paged
+    assert idx_paged(P, P, P, P, P, None, 4, 64, 8, 1, 1, 256, P, 256, stream) == 1        # no table
+    assert idx_paged(P, P, P, P, P, P, 4, 48, 8, 1, 1, 192, P, 192, stream) == 2           # not a power of two
+    assert idx_paged(P, P, P, P, P, P, 4, 8, 8, 1, 1, 32, P, 32, stream) == 2              # below 16 rows
+    assert idx_paged(P, P, P, P, P, P, 4, 64, 8, 1, 1, 257, P, 260, stream) == 1           # Nmax > 4 pages
+    assert idx_paged(P, P, P, P, P, P, 4, 65536, 1 << 16, 1, 1, 256, P, 256, stream) == 2  # pool rows > 2^31-1
+    assert idx_paged(P, P + 2, P, P, P, P, 4, 64, 8, 1, 1, 256, P, 256, stream) == 3       # k_pool misaligned
+    dec_paged = lib.mla_sparse_attn_decode_paged
+    assert dec_paged(P, P, P, P, 4, 64, 8, P, 8, 256, 2048, 0.0625, P, None, P, ws - 1, stream) == 4
+    assert dec_paged(P, P, P, P, 0, 64, 8, P, 8, 256, 2048, 0.0625, P, None, P, ws, stream) == 1
+    assert dec_paged(P, P, P, P, 4, 100, 8, P, 8, 256, 2048, 0.0625, P, None, P, ws, stream) == 2
+    assert dec_paged(P, P, P, P, 4, 64, 8, P, 8, 256, 0, 0.0625, P, None, P, ws, stream) == 2
     code = ctypes.c_int32(0)
     assert lib.dsa_device_status(None, None, 0) == 1
 

@@ -287,6 +287,76 @@ def test_decode_many_sequences(dsa, oracle_mod):
     run_decode_chain(dsa, oracle_mod, wl, kv_len)
 
 
+# ----------------------------------------------------------------------------- paged caches
+
+def run_paged_decode_chain(dsa, oracle_mod, wl, kv_len, page_size, corrupt=None):
+    """Decode step over paged caches (shuffled pool with unreferenced junk pages); the oracle runs
+    on the dense caches its page lookup rebuilds.  `corrupt` = (b, logical page): that table entry
+    is pointed past the pool, which must be reported and read as zero rows."""
+    qi, ki, w = W.make_indexer_inputs(wl)
+    q, kv = W.make_attention_inputs(wl)
+    kv_len = np.asarray(kv_len, np.int32)
+    q_pos0 = kv_len - 1
+    k_pool, table = W.paginate(ki, kv_len, page_size, extra_pages=5, seed=wl.seed + 1)
+    kv_pool, table2 = W.paginate(kv, kv_len, page_size, extra_pages=5, seed=wl.seed + 1)
+    assert np.array_equal(table, table2)
+    if corrupt is not None:
+        table = table.copy()
+        table[corrupt] = k_pool.shape[0] // page_size
+    d_pos, d_len, d_tab = dev(q_pos0), dev(kv_len), dev(table)
+    S = dsa.indexer_scores_paged(dev(qi), dev(k_pool), dev(w), d_pos, d_len, d_tab, page_size, wl.N)
+    idx = dsa.topk(S, d_pos, d_len, wl.N, wl.top_k)
+    out, lse = dsa.mla_sparse_attn_decode_paged(dev(q[:, 0]), dev(kv_pool), d_len, d_tab, page_size, idx[:, 0],
+                                                W.SCALE, wl.N, want_lse=True)
+    torch.cuda.synchronize()
+    status = dsa.device_status()
+    th = oracle_mod.default_threads()
+    ki_d = oracle_mod.unpage(k_pool, table, page_size, kv_len, wl.N)
+    kv_d = oracle_mod.unpage(kv_pool, table, page_size, kv_len, wl.N)
+    S_ref = oracle_mod.indexer(qi, ki_d, w, q_pos0, kv_len, threads=th)
+    np.testing.assert_array_equal(S[:, 0, : wl.N].cpu().numpy().astype(np.float64), S_ref.reshape(wl.B, wl.N))
+    idx_ref = oracle_mod.topk(S_ref.astype(np.float32), q_pos0, kv_len, wl.B, 1, wl.top_k, threads=th)
+    np.testing.assert_array_equal(idx[:, 0].cpu().numpy(), idx_ref)
+    o_ref, l_ref = oracle_mod.attention(q[:, 0], kv_d, idx_ref, np.arange(wl.B, dtype=np.int32), W.SCALE,
+                                        threads=th)
+    attn_close(out.float().cpu().numpy(), o_ref, f"{wl.name} page {page_size}")
+    np.testing.assert_allclose(lse.cpu().numpy(), l_ref, rtol=1e-5, atol=1e-5)
+    return status
+
+
+@pytest.mark.parametrize("page_size", [16, 64, 128, 1024])
+def test_paged_decode_ragged(dsa, oracle_mod, page_size):
+    """Paged caches of five ragged sequences (full, n < top_k, top_k, top_k + 1, odd length):
+    bit-exact scores and indices, attention within tolerance, for pages smaller than, equal to
+    and larger than the 128-key tile."""
+    wl = W.custom("decode_paged", B=5, L=1, p0=0, N=4096, top_k=2048, seed=51)
+    assert run_paged_decode_chain(dsa, oracle_mod, wl, [4096, 100, 2049, 2048, 3001], page_size) == 0
+
+
+def test_paged_decode_bad_page_is_reported(dsa, oracle_mod):
+    """A table entry past the pool, inside a sequence's keys, is recorded as a bounds error and its
+    rows are read as zeros by both kernels (the oracle's page lookup reads it the same way)."""
+    wl = W.custom("decode_paged_bad", B=3, L=1, p0=0, N=1024, top_k=256, seed=53)
+    assert run_paged_decode_chain(dsa, oracle_mod, wl, [1024, 700, 300], 64, corrupt=(1, 3)) == 7
+
+
+def test_paged_indexer_chunked_prefill(dsa, oracle_mod):
+    """The paged indexer with several queries per sequence (a prefill chunk over a paged
+    cache): two sequences at different positions, bit-exact against the oracle."""
+    wl = W.custom("paged_chunk", B=2, L=40, p0=0, N=1000, top_k=64, seed=55)
+    qi, ki, w = W.make_indexer_inputs(wl)
+    q_pos0 = np.array([960, 300], np.int32)
+    kv_len = np.array([1000, 340], np.int32)
+    k_pool, table = W.paginate(ki, kv_len, 32, extra_pages=4, seed=56)
+    S = dsa.indexer_scores_paged(dev(qi), dev(k_pool), dev(w), dev(q_pos0), dev(kv_len), dev(table), 32, wl.N)
+    torch.cuda.synchronize()
+    ki_d = oracle_mod.unpage(k_pool, table, 32, kv_len, wl.N)
+    ref = oracle_mod.indexer(qi, ki_d, w, q_pos0, kv_len, threads=oracle_mod.default_threads())
+    got = S.cpu().numpy()[:, :, : wl.N].reshape(wl.B * wl.L, wl.N).astype(np.float64)
+    np.testing.assert_array_equal(got, ref)
+    assert dsa.device_status() == 0
+
+
 @pytest.mark.parametrize("slices", [1, 3])
 def test_host_prefill_matches_device_calls(dsa, slices):
     """HostPrefill (pinned host in, pinned host out, copies overlapped) gives the same bits as the

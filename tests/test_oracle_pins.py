@@ -271,3 +271,37 @@ def test_generator_grid_and_ties():
     a, b = W.make_attention_inputs(wl)
     a2, b2 = W.make_attention_inputs(wl)
     assert np.array_equal(a, a2) and np.array_equal(b, b2)
+
+
+# ----------------------------------------------------------------------------- paged caches
+
+def test_unpage_hand_example(oracle_mod):
+    """Pool row r holds the value r (one column); pages of 2 rows.  Sequence 0 has 3 keys in
+    pool pages 3 then 0; sequence 1 has 4 keys in pages 1 then 2; page 4 is never referenced.
+    Worked by hand: keys of sequence 0 are pool rows 6, 7, 0; of sequence 1 rows 2, 3, 4, 5."""
+    pool = np.arange(10, dtype=np.int64).reshape(10, 1)
+    table = np.array([[3, 0], [1, 2]], np.int32)
+    got = oracle_mod.unpage(pool, table, 2, [3, 4], 4)
+    expect = np.array([[[6], [7], [0], [0]], [[2], [3], [4], [5]]])
+    np.testing.assert_array_equal(got, expect)
+    # an entry outside the pool reads as zeros; entries past kv_len are never read
+    bad = np.array([[3, 9], [1, -1]], np.int32)
+    got = oracle_mod.unpage(pool, bad, 2, [3, 2], 4)
+    np.testing.assert_array_equal(got, np.array([[[6], [7], [0], [0]], [[2], [3], [0], [0]]]))
+
+
+def test_paginate_then_unpage_is_identity(oracle_mod):
+    """The seeded page scatter of the input generator and the oracle's page lookup are
+    inverses on every key a sequence holds, for page sizes below, at and above a tile."""
+    rng = np.random.default_rng(5)
+    dense = W.f32_to_bf16_bits(rng.standard_normal((3, 300, 8), dtype=np.float32))
+    kv_len = np.array([300, 17, 129])
+    for ps in (16, 128, 256):
+        pool, table = W.paginate(dense, kv_len, ps, extra_pages=3, seed=ps)
+        assert pool.shape == ((sum(-(-n // ps) for n in kv_len) + 3) * ps, 8)
+        used = table[table >= 0]
+        assert len(set(used.tolist())) == len(used)          # no page shared by two places
+        back = oracle_mod.unpage(pool, table, ps, kv_len, 300)
+        for b, n in enumerate(kv_len):
+            np.testing.assert_array_equal(back[b, :n], dense[b, :n])
+            assert not back[b, n:].any()
