@@ -238,7 +238,8 @@ def config_block(wl, world):
             "q_pos0": wl.p0, "top_k": wl.top_k, "heads": 64, "qk_dim": 576, "v_dim": 512,
             "indexer_heads": 32, "indexer_dim": 128, "global_batch": wl.B * wl.L * world,
             "parallelism": f"replicas{world}" if world > 1 else "single",
-            "l2": "flushed between timed steps (write of a 512 MiB buffer); inputs larger than L2"}
+            "l2": "flushed between timed steps (write of a 512 MiB buffer); inputs larger than L2",
+            **({"page_size": wl.page_size} if wl.page_size else {})}
 
 
 def run_gpu(args, wl, rank, world, local_rank):
@@ -256,6 +257,11 @@ def run_gpu(args, wl, rank, world, local_rank):
         a = np.ascontiguousarray(a)
         return torch.from_numpy(a.view(np.int16) if a.dtype == np.uint16 else a).to(dev)
 
+    if wl.page_size:
+        # paged caches: the same rows, scattered over a shuffled pool of pages
+        ki, table = W.paginate(ki, kv_len, wl.page_size, extra_pages=8, seed=wl.seed + 7)
+        kv, _ = W.paginate(kv, kv_len, wl.page_size, extra_pages=8, seed=wl.seed + 7)
+        dtab = d(table)
     dqi, dki, dw, dpos, dlen, dq, dkv = map(d, (qi, ki, w, q_pos0, kv_len, q, kv))
     ld = (wl.N + 3) // 4 * 4
     S = torch.empty((wl.B, wl.L, ld), dtype=torch.float32, device=dev)
@@ -266,8 +272,17 @@ def run_gpu(args, wl, rank, world, local_rank):
     flush = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream()
 
+    def indexer(a_qi, a_ki, a_w, a_pos, a_len):
+        if wl.page_size:
+            dsa.indexer_scores_paged(a_qi, a_ki, a_w, a_pos, a_len, dtab, wl.page_size, wl.N, scores=S)
+        else:
+            dsa.indexer_scores(a_qi, a_ki, a_w, a_pos, a_len, scores=S)
+
     def attention(a_q, a_kv, a_len):
-        if decode:   # one query per sequence: the batched decode entry point
+        if wl.page_size:
+            dsa.mla_sparse_attn_decode_paged(a_q[:, 0], a_kv, a_len, dtab, wl.page_size, idx[:, 0], W.SCALE,
+                                             wl.N, out=out, workspace=ws)
+        elif decode:   # one query per sequence: the batched decode entry point
             dsa.mla_sparse_attn_decode(a_q[:, 0], a_kv, a_len, idx[:, 0], W.SCALE, out=out, workspace=ws)
         else:
             dsa.mla_sparse_attn_prefill(a_q[0], a_kv[0], idx[0], W.SCALE, out=out)
@@ -275,7 +290,7 @@ def run_gpu(args, wl, rank, world, local_rank):
     def step(ev=None):
         if ev:
             ev[0].record(stream)
-        dsa.indexer_scores(dqi, dki, dw, dpos, dlen, scores=S)
+        indexer(dqi, dki, dw, dpos, dlen)
         if ev:
             ev[1].record(stream)
         dsa.topk(S, dpos, dlen, wl.N, wl.top_k, idx=idx)
@@ -374,7 +389,7 @@ def run_gpu(args, wl, rank, world, local_rank):
             for i in per_step:
                 dev_in[i].copy_(host_in[i], non_blocking=True)
             a_qi, a_ki, a_w, a_pos, a_len, a_q, a_kv = dev_in
-            dsa.indexer_scores(a_qi, a_ki, a_w, a_pos, a_len, scores=S)
+            indexer(a_qi, a_ki, a_w, a_pos, a_len)
             dsa.topk(S, a_pos, a_len, wl.N, wl.top_k, idx=idx)
             attention(a_q, a_kv, a_len)
             host_out.copy_(out, non_blocking=True)

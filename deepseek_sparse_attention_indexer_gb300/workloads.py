@@ -57,6 +57,7 @@ class Workload:
     rope_std: float = 1.0
     dup_frac: float = 0.0
     desc: str = ""
+    page_size: int = 0     # > 0: the caches live in pages of this many rows (see paginate)
 
     @property
     def n_rows(self) -> int:
@@ -82,6 +83,9 @@ WORKLOADS: Dict[str, Workload] = {
     "decode_b1": Workload(
         "decode_b1", B=1, L=1, p0=4095, N=4096, top_k=2048, seed=1024,
         desc="1 sequence, one query at position 4095 over 4096 keys"),
+    "decode_b8_paged": Workload(
+        "decode_b8_paged", B=8, L=1, p0=4095, N=4096, top_k=2048, seed=1004, page_size=64,
+        desc="decode_b8's sequences with their caches in 64-row pages of a shuffled pool"),
     "prefill_64k": Workload(
         "prefill_64k", B=1, L=4096, p0=61440, N=65536, top_k=2048, seed=1005,
         rope_std=0.5, dup_frac=0.05,

@@ -128,7 +128,28 @@ def test_topk_bit_exact_with_ties(dsa, oracle_mod, rows, n, K, p0):
     np.testing.assert_array_equal(idx.cpu().numpy()[0], ref)
 
 
-@pytest.mark.parametrize("n", [4000, 12000])
+@pytest.mark.parametrize("n_tied", [2500, 2584, 2585, 2600])
+def test_topk_long_rows_tie_block_at_list_capacity(dsa, oracle_mod, n_tied):
+    """Rows longer than 16384 keys: 1000 keys above a block of n_tied equal keys that holds the
+    threshold (1048 of them are taken, lowest indices first), the rest below.  Together they fill
+    the long-row candidate list (3584 entries) up to, exactly at, one past and past its capacity,
+    so both the list path and the streaming fallback decide the ties."""
+    n, K, rows = 40000, 2048, 4
+    rng = np.random.default_rng(n_tied)
+    S = rng.uniform(-1.0, 1.0, (rows, n)).astype(np.float32)
+    for r in range(rows):
+        perm = rng.permutation(n)
+        S[r, perm[:1000]] = 10.0 + r
+        S[r, perm[1000:1000 + n_tied]] = 5.0
+    q_pos0 = np.array([n - rows], np.int32)
+    kv_len = np.array([n], np.int32)
+    idx = dsa.topk(dev(S[None]), dev(q_pos0), dev(kv_len), n, K)
+    torch.cuda.synchronize()
+    ref = oracle_mod.topk(S, q_pos0, kv_len, 1, rows, K)
+    np.testing.assert_array_equal(idx.cpu().numpy()[0], ref)
+
+
+@pytest.mark.parametrize("n", [4000, 12000, 20000])
 def test_topk_all_equal_and_signed_zero(dsa, oracle_mod, n):
     K, rows = 2048, 3
     S = np.zeros((rows, n), np.float32)
