@@ -250,6 +250,41 @@ def test_attention_generator_indices_with_gaps(dsa, oracle_mod):
     np.testing.assert_allclose(lse.cpu().numpy()[keep], l_ref[keep], rtol=1e-5, atol=1e-5)
 
 
+@pytest.mark.parametrize("order", ["rising", "falling", "mixed"])
+def test_attention_scores_far_beyond_the_first_tile(dsa, oracle_mod, order):
+    """Score ranges that move by far more than the kernel's rescale threshold (2^16 in exp2 terms)
+    from one 128-key tile to the next: cache rows scaled by up to 2^5, so a query's scaled scores
+    span hundreds of log2 units.  Rising: every later tile raises some head's maximum (the rescale
+    of O and of the row sums runs on most tiles); falling: the first tile holds the maxima and the
+    rest underflow; mixed: both, in random order.  Decode splits merge such partials too."""
+    wl = W.custom("ranges", B=1, L=6, p0=4090, N=4096, top_k=2048, seed=61)
+    q, kv = W.make_attention_inputs(wl)
+    rng = np.random.default_rng(62)
+    idx = np.stack([np.sort(rng.choice(wl.N, size=wl.top_k, replace=False)) for _ in range(wl.L)]).astype(np.int32)
+    kvf = W.bf16_bits_to_f32(kv[0])
+    if order == "rising":
+        gain = 2.0 ** (5.0 * np.arange(wl.N) / wl.N)
+    elif order == "falling":
+        gain = 2.0 ** (5.0 * (1.0 - np.arange(wl.N) / wl.N))
+    else:
+        gain = 2.0 ** rng.uniform(0.0, 5.0, wl.N)
+    kv_big = W.f32_to_bf16_bits((kvf * gain[:, None]).astype(np.float32))[None]
+    out, lse = dsa.mla_sparse_attn_prefill(dev(q[0]), dev(kv_big[0]), dev(idx), W.SCALE, want_lse=True)
+    torch.cuda.synchronize()
+    o_ref, l_ref = oracle_mod.attention(q[0], kv_big, idx, np.zeros(wl.L, np.int32), W.SCALE)
+    attn_close(out.float().cpu().numpy(), o_ref, order)
+    np.testing.assert_allclose(lse.cpu().numpy(), l_ref, rtol=1e-5, atol=1e-3)
+    # the same rows as decode sequences (split over CTAs, partials merged)
+    B = wl.L
+    kv_dec = np.repeat(kv_big, B, axis=0)
+    kv_len = np.full(B, wl.N, np.int32)
+    out_d, lse_d = dsa.mla_sparse_attn_decode(dev(q[0]), dev(kv_dec), dev(kv_len), dev(idx), W.SCALE, want_lse=True)
+    torch.cuda.synchronize()
+    attn_close(out_d.float().cpu().numpy(), o_ref, order + " decode")
+    np.testing.assert_allclose(lse_d.cpu().numpy(), l_ref, rtol=1e-5, atol=1e-3)
+    assert dsa.device_status() == 0
+
+
 def test_attention_out_of_range_index_is_reported(dsa, oracle_mod):
     wl = W.custom("oob", B=1, L=4, p0=200, N=256, top_k=128, seed=5)
     q, kv = W.make_attention_inputs(wl)
