@@ -22,7 +22,10 @@
 //     2..17 run the epilogue, four per TMEM lane quadrant (two of the eight
 //     queries each, one query's 32 head columns per TMEM wait): with four
 //     epilogue warps per scheduler, one warp's TMEM and weight loads hide
-//     behind the others' arithmetic.
+//     behind the others' arithmetic.  The head weights of a warp's first query
+//     stay in registers for the whole item (the second's are re-read per tile:
+//     both do not fit in 96 registers); re-reading every weight on every tile
+//     cost 12% (the broadcast loads, not their latency, measured on GB300).
 //   * Work items are (batch, 8-query group, key chunk); CTAs are persistent and
 //     walk the items in a zig-zag order so the triangular causal workload of a
 //     first chunk spreads evenly.  Key tiles past the group's last causal key
@@ -45,7 +48,6 @@ constexpr int kHi = DSA_INDEXER_HEADS;  // 32
 constexpr int kDi = DSA_INDEXER_DIM;    // 128
 constexpr int kTileKeys = 128;          // MMA M
 constexpr int kEpiWarps = 16;           // four per TMEM lane quadrant
-constexpr int kQPerWait = (kEpiWarps >= 16) ? 1 : 2;   // queries whose TMEM columns one wait covers
 constexpr int kThreads = (2 + kEpiWarps) * 32;   // 576: 18 warps, at most 96 registers a thread
 
 struct IndexerParams {
@@ -99,6 +101,19 @@ __device__ __forceinline__ float weighted_relu_sum(const uint32_t (&x)[32], cons
                        make_float2(fmaxf(__uint_as_float(x[4 * h4 + 2]), 0.f), fmaxf(__uint_as_float(x[4 * h4 + 3]), 0.f)),
                        s);
         asm volatile("" ::: "memory");   // keep each weight load next to its use (register pressure)
+    }
+    return s.x + s.y;
+}
+
+// The same sum with the query's 32 head weights already in registers (same order).
+__device__ __forceinline__ float weighted_relu_sum_reg(const uint32_t (&x)[32], const float4 (&wv)[kHi / 4]) {
+    float2 s = make_float2(0.f, 0.f);
+#pragma unroll
+    for (int h4 = 0; h4 < kHi / 4; ++h4) {
+        s = __ffma2_rn(make_float2(wv[h4].x, wv[h4].y),
+                       make_float2(fmaxf(__uint_as_float(x[4 * h4 + 0]), 0.f), fmaxf(__uint_as_float(x[4 * h4 + 1]), 0.f)), s);
+        s = __ffma2_rn(make_float2(wv[h4].z, wv[h4].w),
+                       make_float2(fmaxf(__uint_as_float(x[4 * h4 + 2]), 0.f), fmaxf(__uint_as_float(x[4 * h4 + 3]), 0.f)), s);
     }
     return s.x + s.y;
 }
@@ -273,9 +288,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         }
     } else {
-        // ------------------------------------------------------------ epilogue (warps 2..9)
+        // ------------------------------------------------------------ epilogue (warps 2..17)
         // kEpiWarps / 4 warps per TMEM lane quadrant; each takes its share of the
-        // group's queries and reads kQPerWait queries' 32 head columns per TMEM wait.
+        // group's queries (two of the eight), one query's 32 head columns per TMEM wait.
         const int e = warp - 2;                      // 0..kEpiWarps-1
         const int quad = warp & 3;                   // TMEM lane quadrant of this warp
         constexpr int kPerQuad = kEpiWarps / 4;
@@ -292,45 +307,45 @@ __global__ void __launch_bounds__(kThreads, 1)
             Item I = decode_item(p, item, QG);
             const int64_t row0 = (int64_t)I.b * p.L + I.i0;
             const int q_end = min(qbase + QW, I.nq);     // this warp's queries are [qbase, q_end)
+            // The first query's head weights stay in registers for the whole item (the
+            // second's are read per tile: both would not fit in 96 registers).
+            float4 w_first[kHi / 4];
+            {
+                const float4* wq = reinterpret_cast<const float4*>(p.w + (row0 + qbase) * kHi);
+#pragma unroll
+                for (int h4 = 0; h4 < kHi / 4; ++h4)
+                    w_first[h4] = (qbase < q_end) ? __ldg(wq + h4) : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+            const float4* w_rest = reinterpret_cast<const float4*>(p.w + (row0 + qbase) * kHi);
+            int lim[QW];   // last causal key of each of the warp's queries
+#pragma unroll
+            for (int qi = 0; qi < QW; ++qi)
+                lim[qi] = (int)min((long long)I.pos0 + I.i0 + qbase + qi, (long long)I.kl - 1);
+            float* srow_item = p.scores + (row0 + qbase) * p.ld + key_in_tile;
             for (int t = I.t_begin; t < I.t_end; ++t) {
                 const int j = t * kTileKeys + key_in_tile;
-                float* srow = p.scores + row0 * p.ld + j;
+                float* srow = srow_item + t * kTileKeys;   // query qbase + qi at srow[qi * ld]
                 if (t < I.n_comp_end) {
                     const int acc = acc_it & 1;
                     if (!(ok = mbar_wait(&acc_full[acc], (acc_it >> 1) & 1, abort_flag, p.status))) break;
                     tc_fence_after();
-                    const float4* w4 = reinterpret_cast<const float4*>(p.w + row0 * kHi);
-#pragma unroll 1
-                    for (int q = qbase; q < qbase + QW; q += kQPerWait) {
-                        if (q >= QG) break;  // warp-uniform: no TMEM columns of this warp's share exist
-                        // kQPerWait queries' 32 head columns per TMEM wait
-                        uint32_t v0[32], v1[32];   // v1 unused (and eliminated) when one query per wait
-                        tmem_ld32(tmem_base + lane_addr + acc * C::N + q * kHi, v0);
-                        if constexpr (kQPerWait == 2) {
-                            if (QG > 1) tmem_ld32(tmem_base + lane_addr + acc * C::N + (q + 1) * kHi, v1);
-                        }
-                        tmem_ld_wait();
-                        const float r0 = (q < q_end) ? weighted_relu_sum(v0, w4 + q * (kHi / 4)) : 0.f;
-                        float r1 = 0.f;
-                        if constexpr (kQPerWait == 2) {
-                            if (QG > 1 && q + 1 < q_end) r1 = weighted_relu_sum(v1, w4 + (q + 1) * (kHi / 4));
-                        }
-                        if (j < p.Nmax) {
-                            if (q < q_end) {
-                                const long long lim = min((long long)I.pos0 + I.i0 + q, (long long)I.kl - 1);
-                                srow[(int64_t)q * p.ld] = ((long long)j <= lim) ? r0 : -INFINITY;
-                            }
-                            if (kQPerWait == 2 && QG > 1 && q + 1 < q_end) {
-                                const long long lim = min((long long)I.pos0 + I.i0 + q + 1, (long long)I.kl - 1);
-                                srow[(int64_t)(q + 1) * p.ld] = ((long long)j <= lim) ? r1 : -INFINITY;
-                            }
+#pragma unroll
+                    for (int qi = 0; qi < QW; ++qi) {
+                        const int q = qbase + qi;
+                        if (q < QG) {   // warp-uniform: TMEM columns of this query exist
+                            uint32_t v0[32];
+                            tmem_ld32(tmem_base + lane_addr + acc * C::N + q * kHi, v0);
+                            tmem_ld_wait();
+                            const float r0 = (qi == 0) ? weighted_relu_sum_reg(v0, w_first)
+                                                       : weighted_relu_sum(v0, w_rest + qi * (kHi / 4));
+                            if (j < p.Nmax && q < q_end) srow[(int64_t)qi * p.ld] = (j <= lim[qi]) ? r0 : -INFINITY;
                         }
                     }
                     tc_fence_before();
                     mbar_arrive(&acc_empty[acc]);
                     ++acc_it;
                 } else if (j < p.Nmax) {
-                    for (int q = qbase; q < q_end; ++q) srow[(int64_t)q * p.ld] = -INFINITY;
+                    for (int q = qbase; q < q_end; ++q) srow[(int64_t)(q - qbase) * p.ld] = -INFINITY;
                 }
             }
         }
