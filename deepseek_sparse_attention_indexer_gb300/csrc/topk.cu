@@ -15,10 +15,11 @@
 //     with block-wide prefix sums: every key above T, plus the first `need`
 //     keys equal to T (this is the lower-index tie rule).  Positions come from
 //     the prefix sums, so the output is ascending without a sort.
-//   * Calls with 8192 < Nmax <= 16384: a thread holds a contiguous run of 32
-//     keys of the row in registers, loaded once from HBM with all of its loads
-//     in flight, for every pass; one block scan orders the compaction.  Two
-//     CTAs per SM.
+//   * Calls with Nmax <= 4096 (eight keys a thread, four CTAs per SM) and
+//     8192 < Nmax <= 16384 (32 keys a thread, two CTAs per SM): a thread
+//     holds a contiguous run of keys of the row in registers, loaded once from
+//     HBM with all of its loads in flight, for every pass; one block scan
+//     orders the compaction.
 //   * Other sizes stream the row on every pass (the first pass reads HBM, later
 //     passes mostly hit L2) with four CTAs per SM: the passes are latency
 //     bound, and more rows in flight win for short rows, while long rows do
@@ -128,24 +129,30 @@ constexpr int kChunk = kThreads * kPer;         // 16384 keys: one block-wide ch
 // Below this many keys a row is short enough that four streaming CTAs per SM
 // (more rows in flight) beat two register-resident ones (measured on GB300).
 constexpr int kRegMinKeys = 8192;
+// Rows of at most 4096 keys: eight keys a thread (one 512-thread block holds the
+// row in registers) at four CTAs per SM beat the streaming kernel (GB300: 4096
+// rows of the first 4k chunk 48.8 -> 41.6 us, a batch-8 decode step's 13 -> 11 us).
+constexpr int kShortPer = 8;
+constexpr int kShortKeys = kThreads * kShortPer;
 // Streaming kernel shapes: kU = float4 loads a thread keeps in flight in a
 // histogram pass, kC = float4 a thread compacts per block scan (4 kC <= 32 mask
 // bits).  Long rows take (4, 8); short rows (one or two block steps) are faster
 // with (1, 1), where every thread has data in every step (measured on GB300).
 constexpr int kLongU = 4, kLongC = 8;
 
-// Load this thread's run of chunk `ch` of the row (keys 32 t .. 32 t + 31 of
-// the chunk) as order keys; positions past the row get key 0 (no finite or
-// infinite score maps to 0).  The eight float4 loads are issued together and
-// go through L1, which keeps the 128-byte lines the warp's strided accesses touch.
-__device__ __forceinline__ void load_run(const float4* row4, int n, int ch, uint32_t (&key)[kPer]) {
-    const int v0 = (ch * kChunk) / 4 + threadIdx.x * (kPer / 4);
+// Load this thread's run of the row (keys PER t .. PER t + PER - 1) as order
+// keys; positions past the row get key 0 (no finite or infinite score maps to
+// 0).  The float4 loads are issued together and go through L1, which keeps the
+// 128-byte lines the warp's strided accesses touch.
+template <int PER>
+__device__ __forceinline__ void load_run(const float4* row4, int n, uint32_t (&key)[PER]) {
+    const int v0 = threadIdx.x * (PER / 4);
     const int n4 = (n + 3) / 4;
-    float4 f[kPer / 4];
+    float4 f[PER / 4];
 #pragma unroll
-    for (int c = 0; c < kPer / 4; ++c) f[c] = (v0 + c < n4) ? __ldg(row4 + v0 + c) : make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int c = 0; c < PER / 4; ++c) f[c] = (v0 + c < n4) ? __ldg(row4 + v0 + c) : make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-    for (int c = 0; c < kPer / 4; ++c) {
+    for (int c = 0; c < PER / 4; ++c) {
         const float e[4] = {f[c].x, f[c].y, f[c].z, f[c].w};
 #pragma unroll
         for (int k = 0; k < 4; ++k) key[4 * c + k] = (4 * (v0 + c) + k < n) ? order_key(e[k]) : 0u;
@@ -391,7 +398,8 @@ __global__ void __launch_bounds__(kThreads, 4) topk_stream_kernel(const TopkPara
 
 // Register-resident select for rows of up to one chunk (16384 keys): the row
 // is loaded once and stays in registers for every pass (two CTAs per SM).
-__global__ void __launch_bounds__(kThreads, 2) topk_reg_kernel(const TopkParams p) {
+template <int PER, int MINB>
+__global__ void __launch_bounds__(kThreads, MINB) topk_reg_kernel(const TopkParams p) {
     __shared__ uint32_t hist[kBins];
     __shared__ uint32_t warp_sums[kWarps + 1];
     __shared__ uint32_t sel[3];
@@ -406,8 +414,8 @@ __global__ void __launch_bounds__(kThreads, 2) topk_reg_kernel(const TopkParams 
             continue;
         }
         const float4* row4 = reinterpret_cast<const float4*>(p.scores + (int64_t)r * p.ld);
-        uint32_t key[kPer];
-        load_run(row4, n, 0, key);
+        uint32_t key[PER];
+        load_run<PER>(row4, n, key);
 
         // ---- radix narrowing: (shift, prefix, need) describe the threshold class
         int shift = 32;        // keys compared on bits [shift, 32); 32 = nothing fixed yet
@@ -421,7 +429,7 @@ __global__ void __launch_bounds__(kThreads, 2) topk_reg_kernel(const TopkParams 
             for (int k = threadIdx.x; k < nbins; k += kThreads) hist[k] = 0u;
             __syncthreads();
 #pragma unroll
-            for (int k = 0; k < kPer; ++k) {
+            for (int k = 0; k < PER; ++k) {
                 const uint32_t kk = key[k];
                 const bool in_class = (shift == 32) || ((kk >> shift) == prefix);
                 if (kk != 0u && in_class) atomicAdd(&hist[(kk >> new_shift) & (uint32_t)(nbins - 1)], 1u);
@@ -441,7 +449,7 @@ __global__ void __launch_bounds__(kThreads, 2) topk_reg_kernel(const TopkParams 
         {
             uint32_t gmask = 0, emask = 0;
 #pragma unroll
-            for (int k = 0; k < kPer; ++k) {
+            for (int k = 0; k < PER; ++k) {
                 const uint32_t kk = key[k];
                 const uint32_t sk = kk >> shift;
                 if (kk != 0u && sk > prefix) gmask |= 1u << k;
@@ -453,7 +461,7 @@ __global__ void __launch_bounds__(kThreads, 2) topk_reg_kernel(const TopkParams 
             (void)total;
             uint32_t g_before = pre & 0xFFFFu;
             uint32_t e_before = pre >> 16;
-            const int j0 = threadIdx.x * kPer;
+            const int j0 = threadIdx.x * PER;
             while (gmask | emask) {
                 const int k = __ffs(gmask | emask) - 1;
                 const uint32_t bit = 1u << k;
@@ -479,9 +487,14 @@ dsa_status_t launch_topk(const float* scores, int64_t ld, const int32_t* q_pos0,
                          int L, int Nmax, int top_k, int32_t* idx, cudaStream_t stream) {
     TopkParams p{scores, ld, q_pos0, kv_len, idx, B, L, Nmax, top_k};
     const long long R = (long long)B * L;
-    if (Nmax > kRegMinKeys && Nmax <= kChunk) {
+    if (Nmax <= kShortKeys) {
+        const int grid = (int)min(R, (long long)device_sm_count() * 4);
+        if (launch_pdl(topk_reg_kernel<kShortPer, 4>, dim3(grid), dim3(kThreads), 0, stream, p) != cudaSuccess)
+            return DSA_ERR_CUDA;
+    } else if (Nmax > kRegMinKeys && Nmax <= kChunk) {
         const int grid = (int)min(R, (long long)device_sm_count() * 2);
-        if (launch_pdl(topk_reg_kernel, dim3(grid), dim3(kThreads), 0, stream, p) != cudaSuccess) return DSA_ERR_CUDA;
+        if (launch_pdl(topk_reg_kernel<kPer, 2>, dim3(grid), dim3(kThreads), 0, stream, p) != cudaSuccess)
+            return DSA_ERR_CUDA;
     } else {
         const int grid = (int)min(R, (long long)device_sm_count() * 4);
         const cudaError_t e =

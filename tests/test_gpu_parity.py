@@ -110,8 +110,10 @@ def test_indexer_full_size_sampled(dsa, oracle_mod, name):
 
 # ----------------------------------------------------------------------------- top-k
 
-# Calls with 8192 < Nmax <= 16384 take the register-resident kernel, other sizes the streaming one.
+# Calls with Nmax <= 4096 or 8192 < Nmax <= 16384 take the register-resident kernel (8 or 32 keys a
+# thread), other sizes the streaming one (candidate list for rows over 16384 keys).
 @pytest.mark.parametrize("rows,n,K,p0", [(64, 5000, 100, 4936), (33, 3000, 2048, 0), (16, 70000, 2048, 69984),
+                                         (50, 4096, 2048, 4046), (20, 4096, 300, 4076), (9, 1500, 700, 1491),
                                          (40, 2100, 2048, 2000), (8, 300, 1, 292),
                                          (48, 12000, 2048, 11952), (24, 16384, 2048, 16360),
                                          (41, 9001, 2048, 8960), (30, 16000, 1, 15970), (6, 10000, 2048, 0)])
