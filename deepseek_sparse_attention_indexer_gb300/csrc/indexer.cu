@@ -8,25 +8,25 @@
 //
 // How (GB300 design):
 //   * One tcgen05 MMA per key tile: M = 128 keys (the A operand, streamed by
-//     TMA through a 4-stage ring), N = 8 queries x 32 heads = 256 (the B
+//     TMA through a 4-stage ring), N = 4 queries x 32 heads = 128 (the B
 //     operand, the group's indexer queries, resident while the CTA walks its
 //     key range), K = 128 (head dim).  The accumulator D[key, (q,h)] lands in
-//     TMEM, double-buffered (2 x 256 columns), so the MMA of tile t+1 overlaps
-//     the epilogue of tile t.
+//     TMEM, four deep (4 x 128 columns), so the MMAs run up to three tiles
+//     ahead of the epilogue.
 //   * Because the keys sit on the TMEM lanes, the 32-head reduction of one
 //     (query, key) score lives entirely inside one thread: 32 columns of its
 //     lane, relu, times the head weight, summed -- no cross-thread traffic and
 //     no per-head [L, N] tensor ever exists.  Each warp then stores 32
 //     consecutive keys of a score row (128-byte coalesced stores).
 //   * Warp roles: warp 0 issues TMA, warp 1 issues the MMAs (one thread), warps
-//     2..17 run the epilogue, four per TMEM lane quadrant (two of the eight
-//     queries each, one query's 32 head columns per TMEM wait): with four
-//     epilogue warps per scheduler, one warp's TMEM and weight loads hide
-//     behind the others' arithmetic.  The head weights of a warp's first query
-//     stay in registers for the whole item (the second's are re-read per tile:
-//     both do not fit in 96 registers); re-reading every weight on every tile
-//     cost 12% (the broadcast loads, not their latency, measured on GB300).
-//   * Work items are (batch, 8-query group, key chunk); CTAs are persistent and
+//     2..17 run the epilogue, four per TMEM lane quadrant, one query each:
+//     with four epilogue warps per scheduler, one warp's TMEM loads hide
+//     behind the others' arithmetic, and a warp's query keeps its 32 head
+//     weights in registers for the whole item.  (Eight-query groups, N = 256,
+//     read each key tile half as often but give a warp two queries, whose 64
+//     weights do not fit in 96 registers: re-reading them, as broadcast loads,
+//     on every tile made those groups 18-22% slower on GB300.)
+//   * Work items are (batch, 4-query group, key chunk); CTAs are persistent and
 //     walk the items in a zig-zag order so the triangular causal workload of a
 //     first chunk spreads evenly.  Key tiles past the group's last causal key
 //     issue no MMA: the epilogue only writes -inf there.
@@ -47,7 +47,7 @@ namespace {
 constexpr int kHi = DSA_INDEXER_HEADS;  // 32
 constexpr int kDi = DSA_INDEXER_DIM;    // 128
 constexpr int kTileKeys = 128;          // MMA M
-constexpr int kEpiWarps = 16;           // four per TMEM lane quadrant
+constexpr int kEpiWarps = 16;           // four per TMEM lane quadrant, one query each
 constexpr int kThreads = (2 + kEpiWarps) * 32;   // 576: 18 warps, at most 96 registers a thread
 
 struct IndexerParams {
@@ -74,12 +74,13 @@ struct Cfg {
     static constexpr int A_BYTES = 2 * A_HALF;              // 32 KB
     static constexpr int B_HALF = N * 64 * 2;               // N rows x 64 dims
     static constexpr int B_BYTES = 2 * B_HALF;
-    static constexpr int TMEM_COLS = (2 * N < 32) ? 32 : 2 * N;
+    static constexpr int NACC = (512 / N >= 4) ? 4 : 2;                 // TMEM accumulators in flight
+    static constexpr int TMEM_COLS = (NACC * N < 32) ? 32 : NACC * N;
     static constexpr int OFF_A = 0;
     static constexpr int OFF_B = STAGES * A_BYTES;
     static constexpr int OFF_BAR = OFF_B + B_BYTES;
-    // barriers: a_full[S], a_empty[S], b_full, b_empty, acc_full[2], acc_empty[2]
-    static constexpr int N_BARS = 2 * STAGES + 6;
+    // barriers: a_full[S], a_empty[S], b_full, b_empty, acc_full[NACC], acc_empty[NACC]
+    static constexpr int N_BARS = 2 * STAGES + 2 + 2 * NACC;
     static constexpr int OFF_TMEM = OFF_BAR + N_BARS * 8;
     static constexpr int OFF_ABORT = OFF_TMEM + 4;
     static constexpr int SMEM = OFF_ABORT + 4 + 1024;  // + slack for 1024-byte alignment
@@ -87,26 +88,10 @@ struct Cfg {
 };
 
 // One query's score for this thread's key: sum over the 32 heads of
-// w[h] * relu(x[h]), x = the head's 32 TMEM columns.  Even heads accumulate in
-// .x and odd heads in .y of a packed f32x2 FMA; the two halves are added last.
-__device__ __forceinline__ float weighted_relu_sum(const uint32_t (&x)[32], const float4* wq) {
-    float2 s = make_float2(0.f, 0.f);
-#pragma unroll
-    for (int h4 = 0; h4 < kHi / 4; ++h4) {
-        const float4 wv = __ldg(wq + h4);
-        s = __ffma2_rn(make_float2(wv.x, wv.y),
-                       make_float2(fmaxf(__uint_as_float(x[4 * h4 + 0]), 0.f), fmaxf(__uint_as_float(x[4 * h4 + 1]), 0.f)),
-                       s);
-        s = __ffma2_rn(make_float2(wv.z, wv.w),
-                       make_float2(fmaxf(__uint_as_float(x[4 * h4 + 2]), 0.f), fmaxf(__uint_as_float(x[4 * h4 + 3]), 0.f)),
-                       s);
-        asm volatile("" ::: "memory");   // keep each weight load next to its use (register pressure)
-    }
-    return s.x + s.y;
-}
-
-// The same sum with the query's 32 head weights already in registers (same order).
-__device__ __forceinline__ float weighted_relu_sum_reg(const uint32_t (&x)[32], const float4 (&wv)[kHi / 4]) {
+// w[h] * relu(x[h]), x = the head's 32 TMEM columns, w in registers.  Even
+// heads accumulate in .x and odd heads in .y of a packed f32x2 FMA; the two
+// halves are added last.
+__device__ __forceinline__ float weighted_relu_sum(const uint32_t (&x)[32], const float4 (&wv)[kHi / 4]) {
     float2 s = make_float2(0.f, 0.f);
 #pragma unroll
     for (int h4 = 0; h4 < kHi / 4; ++h4) {
@@ -166,7 +151,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t* b_full = bars + 2 * STAGES;
     uint64_t* b_empty = b_full + 1;
     uint64_t* acc_full = b_full + 2;
-    uint64_t* acc_empty = b_full + 4;
+    uint64_t* acc_empty = b_full + 2 + C::NACC;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_TMEM);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_ABORT);
 
@@ -180,7 +165,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         mbar_init(b_full, 1);
         mbar_init(b_empty, 1);
-        for (int a = 0; a < 2; ++a) {
+        for (int a = 0; a < C::NACC; ++a) {
             mbar_init(&acc_full[a], 1);
             mbar_init(&acc_empty[a], kEpiWarps * 32);
         }
@@ -266,9 +251,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint32_t b_base = smem_u32(sB);
                 for (int t = I.t_begin; t < I.n_comp_end; ++t, ++it, ++acc_it) {
                     const int st = it % STAGES;
-                    const int acc = acc_it & 1;
+                    const int acc = acc_it % C::NACC;
                     if (!(ok = mbar_wait_spin(&a_full[st], (it / STAGES) & 1, abort_flag, p.status))) break;
-                    if (!(ok = mbar_wait_spin(&acc_empty[acc], ((acc_it >> 1) & 1) ^ 1, abort_flag, p.status))) break;
+                    if (!(ok = mbar_wait_spin(&acc_empty[acc], ((acc_it / C::NACC) & 1) ^ 1, abort_flag, p.status))) break;
                     tc_fence_after();
                     const uint32_t a_base = smem_u32(sA + st * C::A_BYTES);
                     const uint32_t d = tmem_base + acc * C::N;
@@ -289,13 +274,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else {
         // ------------------------------------------------------------ epilogue (warps 2..17)
-        // kEpiWarps / 4 warps per TMEM lane quadrant; each takes its share of the
-        // group's queries (two of the eight), one query's 32 head columns per TMEM wait.
+        // kEpiWarps / 4 warps per TMEM lane quadrant, one of the group's queries
+        // each (warps whose query is past the group's end only write -inf).
+        static_assert(QG <= kEpiWarps / 4, "one query per epilogue warp");
         const int e = warp - 2;                      // 0..kEpiWarps-1
         const int quad = warp & 3;                   // TMEM lane quadrant of this warp
-        constexpr int kPerQuad = kEpiWarps / 4;
-        constexpr int QW = (QG + kPerQuad - 1) / kPerQuad;   // queries per warp (may be none)
-        const int qbase = (e >> 2) * QW;
+        const int q = e >> 2;                        // this warp's query within the group
         const int key_in_tile = quad * 32 + (int)lane;
         const uint32_t lane_addr = static_cast<uint32_t>(quad * 32) << 16;
         int acc_it = 0;
@@ -306,46 +290,35 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (item < 0) continue;
             Item I = decode_item(p, item, QG);
             const int64_t row0 = (int64_t)I.b * p.L + I.i0;
-            const int q_end = min(qbase + QW, I.nq);     // this warp's queries are [qbase, q_end)
-            // The first query's head weights stay in registers for the whole item (the
-            // second's are read per tile: both would not fit in 96 registers).
-            float4 w_first[kHi / 4];
+            const bool mine = q < I.nq;               // warp-uniform
+            // the query's 32 head weights, in registers for the whole item
+            float4 wq[kHi / 4];
             {
-                const float4* wq = reinterpret_cast<const float4*>(p.w + (row0 + qbase) * kHi);
+                const float4* w4 = reinterpret_cast<const float4*>(p.w + (row0 + q) * kHi);
 #pragma unroll
-                for (int h4 = 0; h4 < kHi / 4; ++h4)
-                    w_first[h4] = (qbase < q_end) ? __ldg(wq + h4) : make_float4(0.f, 0.f, 0.f, 0.f);
+                for (int h4 = 0; h4 < kHi / 4; ++h4) wq[h4] = mine ? __ldg(w4 + h4) : make_float4(0.f, 0.f, 0.f, 0.f);
             }
-            const float4* w_rest = reinterpret_cast<const float4*>(p.w + (row0 + qbase) * kHi);
-            int lim[QW];   // last causal key of each of the warp's queries
-#pragma unroll
-            for (int qi = 0; qi < QW; ++qi)
-                lim[qi] = (int)min((long long)I.pos0 + I.i0 + qbase + qi, (long long)I.kl - 1);
-            float* srow_item = p.scores + (row0 + qbase) * p.ld + key_in_tile;
+            const int lim = (int)min((long long)I.pos0 + I.i0 + q, (long long)I.kl - 1);   // last causal key
+            float* srow_item = p.scores + (row0 + q) * p.ld + key_in_tile;
             for (int t = I.t_begin; t < I.t_end; ++t) {
                 const int j = t * kTileKeys + key_in_tile;
-                float* srow = srow_item + t * kTileKeys;   // query qbase + qi at srow[qi * ld]
+                float* srow = srow_item + t * kTileKeys;
                 if (t < I.n_comp_end) {
-                    const int acc = acc_it & 1;
-                    if (!(ok = mbar_wait(&acc_full[acc], (acc_it >> 1) & 1, abort_flag, p.status))) break;
+                    const int acc = acc_it % C::NACC;
+                    if (!(ok = mbar_wait(&acc_full[acc], (acc_it / C::NACC) & 1, abort_flag, p.status))) break;
                     tc_fence_after();
-#pragma unroll
-                    for (int qi = 0; qi < QW; ++qi) {
-                        const int q = qbase + qi;
-                        if (q < QG) {   // warp-uniform: TMEM columns of this query exist
-                            uint32_t v0[32];
-                            tmem_ld32(tmem_base + lane_addr + acc * C::N + q * kHi, v0);
-                            tmem_ld_wait();
-                            const float r0 = (qi == 0) ? weighted_relu_sum_reg(v0, w_first)
-                                                       : weighted_relu_sum(v0, w_rest + qi * (kHi / 4));
-                            if (j < p.Nmax && q < q_end) srow[(int64_t)qi * p.ld] = (j <= lim[qi]) ? r0 : -INFINITY;
-                        }
+                    if (q < QG) {   // warp-uniform: TMEM columns of this query exist
+                        uint32_t v[32];
+                        tmem_ld32(tmem_base + lane_addr + acc * C::N + q * kHi, v);
+                        tmem_ld_wait();
+                        const float r = weighted_relu_sum(v, wq);
+                        if (j < p.Nmax && mine) *srow = (j <= lim) ? r : -INFINITY;
                     }
                     tc_fence_before();
                     mbar_arrive(&acc_empty[acc]);
                     ++acc_it;
-                } else if (j < p.Nmax) {
-                    for (int q = qbase; q < q_end; ++q) srow[(int64_t)(q - qbase) * p.ld] = -INFINITY;
+                } else if (j < p.Nmax && mine) {
+                    *srow = -INFINITY;
                 }
             }
         }
@@ -380,7 +353,7 @@ dsa_status_t launch_impl(const void* q_idx, const void* k_idx, const IndexerPara
 dsa_status_t launch_indexer(const void* q_idx, const void* k_idx, const float* w, const int32_t* q_pos0,
                             const int32_t* kv_len, int B, int L, int Nmax, float* scores, int64_t ld,
                             const PageTable& pages, cudaStream_t stream) {
-    const int QG = (L == 1) ? 1 : 8;
+    const int QG = (L == 1) ? 1 : 4;
     IndexerParams p;
     p.w = w;
     p.q_pos0 = q_pos0;
@@ -407,7 +380,7 @@ dsa_status_t launch_indexer(const void* q_idx, const void* k_idx, const float* w
     p.status = device_status_ptr();
     p.pages = pages;
     p.box_rows = pages.table ? (pages.shift >= 7 ? kTileKeys : (1 << pages.shift)) : kTileKeys;
-    if (QG == 8) return launch_impl<8, 4>(q_idx, k_idx, p, B, L, Nmax, stream);
+    if (QG == 4) return launch_impl<4, 4>(q_idx, k_idx, p, B, L, Nmax, stream);
     return launch_impl<1, 4>(q_idx, k_idx, p, B, L, Nmax, stream);
 }
 
