@@ -15,8 +15,8 @@
 //     with block-wide prefix sums: every key above T, plus the first `need`
 //     keys equal to T (this is the lower-index tie rule).  Positions come from
 //     the prefix sums, so the output is ascending without a sort.
-//   * Calls with Nmax <= 4096 (eight keys a thread, four CTAs per SM) and
-//     8192 < Nmax <= 16384 (32 keys a thread, two CTAs per SM): a thread
+//   * Calls with Nmax <= 4096 (512 threads of eight keys, four CTAs per SM)
+//     and 8192 < Nmax <= 16384 (1024 threads of 16 keys, two CTAs per SM): a thread
 //     holds a contiguous run of keys of the row in registers, loaded once from
 //     HBM with all of its loads in flight, for every pass; one block scan
 //     orders the compaction.
@@ -56,9 +56,13 @@ __device__ __forceinline__ uint32_t order_key(float f) {
     return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
-// Block-wide exclusive scan of one uint32 per thread; returns the exclusive
-// prefix and writes the block total to *total.  Uses warp_sums[kWarps + 1].
+// Block-wide exclusive scan of one uint32 per thread (NT threads); returns the
+// exclusive prefix and writes the block total to *total.  Uses
+// warp_sums[NT / 32 + 1].
+template <int NT = kThreads>
 __device__ __forceinline__ uint32_t block_excl_scan(uint32_t v, uint32_t* warp_sums, uint32_t* total) {
+    constexpr int kWarps = NT / 32;
+    static_assert(kWarps <= 32, "one warp scans the warp sums");
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     uint32_t x = v;
 #pragma unroll
@@ -88,8 +92,9 @@ __device__ __forceinline__ uint32_t block_excl_scan(uint32_t v, uint32_t* warp_s
 // Given hist[nbins] of the still-tied keys and `need` (>= 1, <= their count),
 // find the bin B* (scanning from the largest bin down) holding the need-th
 // largest key.  Writes sel[0] = B*, sel[1] = need minus the keys in bins above.
+template <int NT = kThreads>
 __device__ void find_bin(const uint32_t* hist, int nbins, uint32_t need, uint32_t* warp_sums, uint32_t* sel) {
-    const int per = nbins / kThreads;  // 8 for 4096 bins, 1 for 256 bins (others idle)
+    const int per = nbins / NT;  // 8 for 4096 bins and 512 threads; 0 for 256 bins (then one bin a thread)
     uint32_t local = 0;
     const int t = threadIdx.x;
     const bool active = (per > 0) ? true : (t < nbins);
@@ -98,7 +103,7 @@ __device__ void find_bin(const uint32_t* hist, int nbins, uint32_t need, uint32_
     if (active)
         for (int k = 0; k < p; ++k) local += hist[nbins - 1 - (t * p + k)];
     uint32_t total;
-    uint32_t above = block_excl_scan(local, warp_sums, &total);
+    uint32_t above = block_excl_scan<NT>(local, warp_sums, &total);
     if (active && above < need && above + local >= need) {
         uint32_t run = above;
         for (int k = 0; k < p; ++k) {
@@ -124,8 +129,11 @@ __device__ __forceinline__ int row_keys(const TopkParams& p, int r) {
     return (int)max(0LL, min(pos + 1, kl));
 }
 
-constexpr int kPer = 32;                        // keys a thread holds: a contiguous run of the row
-constexpr int kChunk = kThreads * kPer;         // 16384 keys: one block-wide chunk of the row
+// 8192 < Nmax <= 16384: 1024 threads of 16 keys each, two CTAs per SM (512 threads of 32 keys: 3%
+// slower on GB300).
+constexpr int kLongRowThreads = 1024;
+constexpr int kPer = 16;                              // keys a thread holds: a contiguous run of the row
+constexpr int kChunk = kLongRowThreads * kPer;        // 16384 keys: the longest register-resident row
 // Below this many keys a row is short enough that four streaming CTAs per SM
 // (more rows in flight) beat two register-resident ones (measured on GB300).
 constexpr int kRegMinKeys = 8192;
@@ -398,10 +406,10 @@ __global__ void __launch_bounds__(kThreads, 4) topk_stream_kernel(const TopkPara
 
 // Register-resident select for rows of up to one chunk (16384 keys): the row
 // is loaded once and stays in registers for every pass (two CTAs per SM).
-template <int PER, int MINB>
-__global__ void __launch_bounds__(kThreads, MINB) topk_reg_kernel(const TopkParams p) {
+template <int PER, int MINB, int NT = kThreads>
+__global__ void __launch_bounds__(NT, MINB) topk_reg_kernel(const TopkParams p) {
     __shared__ uint32_t hist[kBins];
-    __shared__ uint32_t warp_sums[kWarps + 1];
+    __shared__ uint32_t warp_sums[NT / 32 + 1];
     __shared__ uint32_t sel[3];
 
     griddep_wait();                 // the scores may still be written by the previous kernel
@@ -410,7 +418,7 @@ __global__ void __launch_bounds__(kThreads, MINB) topk_reg_kernel(const TopkPara
         const int n = row_keys(p, r);
         int32_t* out = p.idx + (int64_t)r * p.K;
         if (n <= p.K) {
-            for (int t = threadIdx.x; t < p.K; t += kThreads) out[t] = t < n ? t : -1;
+            for (int t = threadIdx.x; t < p.K; t += NT) out[t] = t < n ? t : -1;
             continue;
         }
         const float4* row4 = reinterpret_cast<const float4*>(p.scores + (int64_t)r * p.ld);
@@ -426,7 +434,7 @@ __global__ void __launch_bounds__(kThreads, MINB) topk_reg_kernel(const TopkPara
             const int bits = digit_bits[pass];
             const int nbins = 1 << bits;
             const int new_shift = shift - bits;
-            for (int k = threadIdx.x; k < nbins; k += kThreads) hist[k] = 0u;
+            for (int k = threadIdx.x; k < nbins; k += NT) hist[k] = 0u;
             __syncthreads();
 #pragma unroll
             for (int k = 0; k < PER; ++k) {
@@ -435,7 +443,7 @@ __global__ void __launch_bounds__(kThreads, MINB) topk_reg_kernel(const TopkPara
                 if (kk != 0u && in_class) atomicAdd(&hist[(kk >> new_shift) & (uint32_t)(nbins - 1)], 1u);
             }
             __syncthreads();
-            find_bin(hist, nbins, need, warp_sums, sel);
+            find_bin<NT>(hist, nbins, need, warp_sums, sel);
             const uint32_t bin = sel[0], rem = sel[1], cnt = sel[2];
             prefix = (shift == 32 ? 0u : (prefix << bits)) | bin;
             shift = new_shift;
@@ -457,7 +465,7 @@ __global__ void __launch_bounds__(kThreads, MINB) topk_reg_kernel(const TopkPara
             }
             const uint32_t packed = ((uint32_t)__popc(emask) << 16) | (uint32_t)__popc(gmask);
             uint32_t total;
-            const uint32_t pre = block_excl_scan(packed, warp_sums, &total);
+            const uint32_t pre = block_excl_scan<NT>(packed, warp_sums, &total);
             (void)total;
             uint32_t g_before = pre & 0xFFFFu;
             uint32_t e_before = pre >> 16;
@@ -493,7 +501,8 @@ dsa_status_t launch_topk(const float* scores, int64_t ld, const int32_t* q_pos0,
             return DSA_ERR_CUDA;
     } else if (Nmax > kRegMinKeys && Nmax <= kChunk) {
         const int grid = (int)min(R, (long long)device_sm_count() * 2);
-        if (launch_pdl(topk_reg_kernel<kPer, 2>, dim3(grid), dim3(kThreads), 0, stream, p) != cudaSuccess)
+        if (launch_pdl(topk_reg_kernel<kPer, 2, kLongRowThreads>, dim3(grid), dim3(kLongRowThreads), 0, stream, p) !=
+            cudaSuccess)
             return DSA_ERR_CUDA;
     } else {
         const int grid = (int)min(R, (long long)device_sm_count() * 4);
