@@ -43,6 +43,7 @@ SIGNATURES = {
     "dsa_indexer_scores_paged": (ctypes.c_int32, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _I64, _P]),
     "mla_sparse_attn_decode_paged": (ctypes.c_int32, [_P, _P, _P, _P, _I, _I, _I, _P, _I, _I, _I, _F, _P, _P, _P,
                                                       _SZ, _P]),
+    "mla_sparse_attn_prefill_paged": (ctypes.c_int32, [_P, _P, _P, _I, _I, _P, _I, _I, _I, _F, _P, _P, _P, _SZ, _P]),
     "dsa_device_status": (ctypes.c_int32, [_P, ctypes.POINTER(ctypes.c_int32), _I]),
 }
 
@@ -241,6 +242,27 @@ def mla_sparse_attn_decode_paged(q: torch.Tensor, kv_pool: torch.Tensor, kv_len:
                                              top_k, float(scale), _ptr(out), _ptr(lse), _ptr(workspace),
                                              workspace.numel(), _stream(stream))
     _check("mla_sparse_attn_decode_paged", rc)
+    return (out, lse) if want_lse else out
+
+
+def mla_sparse_attn_prefill_paged(q: torch.Tensor, kv_pool: torch.Tensor, block_table: torch.Tensor,
+                                  page_size: int, idx: torch.Tensor, scale: float, N: int,
+                                  out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
+                                  want_lse: bool = False, stream=None):
+    """mla_sparse_attn_prefill over one sequence's paged cache: kv_pool [num_pages * page_size, 576]
+    bf16, block_table int32 with ceil(N / page_size) entries; idx holds logical key positions < N."""
+    L = q.shape[0]
+    top_k = idx.shape[-1]
+    assert _is16(q) and _is16(kv_pool) and idx.dtype == torch.int32 and block_table.dtype == torch.int32
+    num_pages = kv_pool.shape[0] // page_size
+    if out is None:
+        out = torch.empty((L, 64, 512), dtype=torch.bfloat16, device=q.device)
+    if lse is None and want_lse:
+        lse = torch.empty((L, 64), dtype=torch.float32, device=q.device)
+    rc = load().mla_sparse_attn_prefill_paged(_ptr(q), _ptr(kv_pool), _ptr(block_table), page_size, num_pages,
+                                              _ptr(idx), L, N, top_k, float(scale), _ptr(out), _ptr(lse), None, 0,
+                                              _stream(stream))
+    _check("mla_sparse_attn_prefill_paged", rc)
     return (out, lse) if want_lse else out
 
 

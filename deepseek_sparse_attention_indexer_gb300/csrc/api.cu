@@ -228,7 +228,28 @@ dsa_status_t mla_sparse_attn_prefill(const void* q, const void* kv, const int32_
     if (!aligned16(q) || !aligned16(kv) || !aligned16(out)) return DSA_ERR_MISALIGNED;
     dsa_status_t st = check_device();
     if (st != DSA_OK) return st;
-    return launch_attn_prefill(q, kv, idx, L, N, top_k, scale, out, lse, static_cast<cudaStream_t>(stream));
+    return launch_attn_prefill(q, kv, idx, L, N, top_k, scale, out, lse, PageTable{}, static_cast<cudaStream_t>(stream));
+}
+
+dsa_status_t mla_sparse_attn_prefill_paged(const void* q, const void* kv_pool, const int32_t* block_table,
+                                           int page_size, int num_pages, const int32_t* idx, int L, int N,
+                                           int top_k, float scale, void* out, float* lse, void* workspace,
+                                           size_t ws_bytes, void* stream) {
+    (void)workspace;
+    (void)ws_bytes;
+    if (!q || !kv_pool || !idx || !out) return DSA_ERR_INVALID_ARG;
+    if (L < 1 || N < 1) return DSA_ERR_INVALID_ARG;
+    if (top_k < 1 || top_k > DSA_MAX_TOPK) return DSA_ERR_UNSUPPORTED_SHAPE;
+    if ((long long)L * DSA_HEADS > 0x7FFFFFFFLL) return DSA_ERR_UNSUPPORTED_SHAPE;
+    if (!(scale > 0.f) || !(scale < 1e30f)) return DSA_ERR_INVALID_ARG;
+    PageTable pt;
+    // one sequence: its table row holds ceil(N / page_size) entries
+    const int stride = page_size > 0 ? (int)(((long long)N + page_size - 1) / page_size) : 0;
+    dsa_status_t st = make_page_table(block_table, stride, page_size, num_pages, N, &pt);
+    if (st != DSA_OK) return st;
+    if (!aligned16(q) || !aligned16(kv_pool) || !aligned16(out)) return DSA_ERR_MISALIGNED;
+    if ((st = check_device()) != DSA_OK) return st;
+    return launch_attn_prefill(q, kv_pool, idx, L, N, top_k, scale, out, lse, pt, static_cast<cudaStream_t>(stream));
 }
 
 dsa_status_t mla_sparse_attn_decode(const void* q, const void* kv, const int32_t* kv_len, const int32_t* idx, int B,

@@ -192,7 +192,7 @@ __device__ __forceinline__ float warp_transpose_reduce16(const float (&x)[16], u
     return MAX ? fmaxf(a[0], o) : a[0] + o;
 }
 
-template <bool PARTIAL>
+template <bool PARTIAL, bool PAGED>
 __global__ void __launch_bounds__(kThreads, 1)   // 18 warps: at most 96 registers a thread (5 warps share one 16K-register SM sub-partition)
     mla_sparse_attn_kernel(const __grid_constant__ CUtensorMap tmap_q, const AttnParams p) {
     extern __shared__ uint8_t smem_raw[];
@@ -376,7 +376,7 @@ __global__ void __launch_bounds__(kThreads, 1)   // 18 warps: at most 96 registe
                 j = -1;
             }
             int64_t prow = (int64_t)gI.batch * p.Nmax + j;   // cache row of key j
-            if (PARTIAL && j >= 0 && p.pages.table != nullptr) {   // paged caches: decode only
+            if (PAGED && j >= 0) {   // paged cache: the row's page from the sequence's table row
                 const int page = __ldg(p.pages.table + (int64_t)gI.batch * p.pages.stride + (j >> p.pages.shift));
                 if (page < 0 || page >= p.pages.num_pages) {
                     raise_dev_error(p.status, DEV_ERR_BOUNDS);
@@ -661,12 +661,12 @@ __global__ void __launch_bounds__(128) mla_decode_combine_kernel(const float* pa
     if (lse && threadIdx.x == 0) lse[(int64_t)b * kH + h] = wsum > 0.f ? M + logf(wsum) : -INFINITY;
 }
 
-template <bool PARTIAL>
+template <bool PARTIAL, bool PAGED>
 dsa_status_t launch_kernel(const void* q, int q_rows, const AttnParams& prm, cudaStream_t stream) {
     CUtensorMap tq;
     dsa_status_t st = make_tmap_bf16_2d(&tq, q, kD, (uint64_t)q_rows * kH, kRowBytes, 64, kH);
     if (st != DSA_OK) return st;
-    auto kern = mla_sparse_attn_kernel<PARTIAL>;
+    auto kern = mla_sparse_attn_kernel<PARTIAL, PAGED>;
     if ((st = ensure_smem_attr(reinterpret_cast<const void*>(kern), SMEM_BYTES)) != DSA_OK) return st;
     const int grid = min(prm.n_items, device_sm_count());
     if (launch_pdl(kern, dim3(grid), dim3(kThreads), SMEM_BYTES, stream, tq, prm) != cudaSuccess) return DSA_ERR_CUDA;
@@ -684,7 +684,7 @@ int decode_splits(int B, int top_k) {
 }  // namespace
 
 dsa_status_t launch_attn_prefill(const void* q, const void* kv, const int32_t* idx, int L, int N, int top_k,
-                                 float scale, void* out, float* lse, cudaStream_t stream) {
+                                 float scale, void* out, float* lse, const PageTable& pages, cudaStream_t stream) {
     AttnParams p{};
     p.kv = static_cast<const __nv_bfloat16*>(kv);
     p.idx = idx;
@@ -700,7 +700,8 @@ dsa_status_t launch_attn_prefill(const void* q, const void* kv, const int32_t* i
     p.n_items = L;
     p.scale_log2 = scale * 1.4426950408889634f;
     p.status = device_status_ptr();
-    return launch_kernel<false>(q, L, p, stream);
+    p.pages = pages;   // a paged cache: batch 0's table row
+    return p.pages.table ? launch_kernel<false, true>(q, L, p, stream) : launch_kernel<false, false>(q, L, p, stream);
 }
 
 size_t attn_decode_workspace(int B, int top_k) {
@@ -730,7 +731,7 @@ dsa_status_t launch_attn_decode(const void* q, const void* kv, const int32_t* kv
     p.scale_log2 = scale * 1.4426950408889634f;
     p.status = device_status_ptr();
     p.pages = pages;
-    dsa_status_t st = launch_kernel<true>(q, B, p, stream);
+    dsa_status_t st = p.pages.table ? launch_kernel<true, true>(q, B, p, stream) : launch_kernel<true, false>(q, B, p, stream);
     if (st != DSA_OK) return st;
     if (launch_pdl(mla_decode_combine_kernel, dim3(B * kH), dim3(128), 0, stream, (const float*)p.part_o,
                    (const float*)p.part_lse, p.nsplit, static_cast<__nv_bfloat16*>(out), lse) != cudaSuccess)
@@ -796,7 +797,7 @@ dsa_status_t launch_attn_decode_noalloc(const void* q, const void* kv, const int
     p.n_items = B * p.nsplit;
     p.scale_log2 = scale * 1.4426950408889634f;
     p.status = device_status_ptr();
-    st = launch_kernel<true>(q, B, p, stream);
+    st = launch_kernel<true, false>(q, B, p, stream);
     if (st != DSA_OK) return st;
     if (launch_pdl(mla_decode_combine_kernel, dim3(B * kH), dim3(128), 0, stream, (const float*)p.part_o,
                    (const float*)p.part_lse, p.nsplit, static_cast<__nv_bfloat16*>(out), lse) != cudaSuccess)

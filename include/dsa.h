@@ -212,7 +212,8 @@ dsa_status_t mla_sparse_attn_decode_noalloc(const void *q, const void *kv, const
  *   k_pool       bf16 [num_pages * page_size, 128]   indexer keys
  *   kv_pool      bf16 [num_pages * page_size, 576]   latent cache rows
  * Any L works for the indexer (chunked prefill over a paged cache as well as
- * decode); the attention call is the decode one (one query per sequence).
+ * decode); attention has a decode call (one query per sequence) and a prefill
+ * call (a chunk of one sequence's queries).
  */
 dsa_status_t dsa_indexer_scores_paged(const void *q_idx, const void *k_pool, const float *w,
                                       const int32_t *q_pos0, const int32_t *kv_len,
@@ -224,6 +225,17 @@ dsa_status_t mla_sparse_attn_decode_paged(const void *q, const void *kv_pool, co
                                           int num_pages, const int32_t *idx, int B, int Nmax,
                                           int top_k, float scale, void *out, float *lse,
                                           void *workspace, size_t ws_bytes, void *stream);
+/* Prefill (a chunk of L queries of one sequence) over that sequence's paged
+ * cache: mla_sparse_attn_prefill with kv[j] = kv_pool[block_table[j / page_size]
+ * * page_size + j % page_size] for the N keys j < N (block_table holds
+ * ceil(N / page_size) entries).  Chunked prefill writes a chunk's keys into the
+ * pool, runs dsa_indexer_scores_paged and dsa_topk for the chunk's queries, then
+ * this call.  Needs no workspace (pass NULL, 0). */
+dsa_status_t mla_sparse_attn_prefill_paged(const void *q, const void *kv_pool,
+                                           const int32_t *block_table, int page_size, int num_pages,
+                                           const int32_t *idx, int L, int N, int top_k, float scale,
+                                           void *out, float *lse, void *workspace, size_t ws_bytes,
+                                           void *stream);
 
 /*
  * dsa_device_status -- synchronise `stream`, then read (and if `reset` is

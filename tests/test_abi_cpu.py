@@ -31,7 +31,8 @@ def test_header_declares_the_path():
     names = declared_functions()
     for n in ["dsa_indexer_scores", "dsa_topk", "mla_sparse_attn_prefill", "mla_sparse_attn_decode",
               "dsa_status_string", "dsa_abi_version", "dsa_device_status", "dsa_topk_workspace_size",
-              "mla_sparse_attn_workspace_size", "dsa_indexer_scores_paged", "mla_sparse_attn_decode_paged"]:
+              "mla_sparse_attn_workspace_size", "dsa_indexer_scores_paged", "mla_sparse_attn_decode_paged",
+              "mla_sparse_attn_prefill_paged"]:
         assert n in names
 
 
@@ -90,6 +91,11 @@ def test_host_validation_rejects_bad_arguments(lib):
     assert dec_paged(P, P, P, P, 0, 64, 8, P, 8, 256, 2048, 0.0625, P, None, P, ws, stream) == 1
     assert dec_paged(P, P, P, P, 4, 100, 8, P, 8, 256, 2048, 0.0625, P, None, P, ws, stream) == 2
     assert dec_paged(P, P, P, P, 4, 64, 8, P, 8, 256, 0, 0.0625, P, None, P, ws, stream) == 2
+    pre_paged = lib.mla_sparse_attn_prefill_paged
+    assert pre_paged(P, P, None, 64, 8, P, 4, 256, 32, 0.0625, P, None, None, 0, stream) == 1       # no table
+    assert pre_paged(P, P, P, 48, 8, P, 4, 256, 32, 0.0625, P, None, None, 0, stream) == 2         # page size
+    assert pre_paged(P, P, P, 64, 8, P, 4, 256, 4096, 0.0625, P, None, None, 0, stream) == 2       # top_k
+    assert pre_paged(P, P + 4, P, 64, 8, P, 4, 256, 32, 0.0625, P, None, None, 0, stream) == 3     # kv_pool
     code = ctypes.c_int32(0)
     assert lib.dsa_device_status(None, None, 0) == 1
 

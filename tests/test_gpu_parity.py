@@ -415,6 +415,36 @@ def test_paged_indexer_chunked_prefill(dsa, oracle_mod):
     assert dsa.device_status() == 0
 
 
+@pytest.mark.parametrize("page_size", [16, 256])
+def test_paged_chunked_prefill_chain(dsa, oracle_mod, page_size):
+    """A prefill chunk of 48 queries (positions 4952..4999) of one sequence whose 5000 keys live in
+    a shuffled page pool: paged indexer, top-k (2048 as on the pages), paged prefill attention,
+    against the oracle on the dense cache its page lookup rebuilds (scores and indices bit-exact)."""
+    wl = W.custom("paged_prefill", B=1, L=48, p0=4952, N=5000, top_k=2048, seed=71)
+    qi, ki, w = W.make_indexer_inputs(wl)
+    q, kv = W.make_attention_inputs(wl)
+    q_pos0, kv_len = W.positions(wl)
+    k_pool, table = W.paginate(ki, kv_len, page_size, extra_pages=3, seed=72)
+    kv_pool, _ = W.paginate(kv, kv_len, page_size, extra_pages=3, seed=72)
+    d_pos, d_len, d_tab = dev(q_pos0), dev(kv_len), dev(table)
+    S = dsa.indexer_scores_paged(dev(qi), dev(k_pool), dev(w), d_pos, d_len, d_tab, page_size, wl.N)
+    idx = dsa.topk(S, d_pos, d_len, wl.N, wl.top_k)
+    out, lse = dsa.mla_sparse_attn_prefill_paged(dev(q[0]), dev(kv_pool), d_tab[0], page_size, idx[0], W.SCALE,
+                                                 wl.N, want_lse=True)
+    torch.cuda.synchronize()
+    th = oracle_mod.default_threads()
+    ki_d = oracle_mod.unpage(k_pool, table, page_size, kv_len, wl.N)
+    kv_d = oracle_mod.unpage(kv_pool, table, page_size, kv_len, wl.N)
+    S_ref = oracle_mod.indexer(qi, ki_d, w, q_pos0, kv_len, threads=th)
+    np.testing.assert_array_equal(S[0, :, : wl.N].cpu().numpy().astype(np.float64), S_ref)
+    idx_ref = oracle_mod.topk(S_ref.astype(np.float32), q_pos0, kv_len, 1, wl.L, wl.top_k, threads=th)
+    np.testing.assert_array_equal(idx[0].cpu().numpy(), idx_ref)
+    o_ref, l_ref = oracle_mod.attention(q[0], kv_d, idx_ref, np.zeros(wl.L, np.int32), W.SCALE, threads=th)
+    attn_close(out.float().cpu().numpy(), o_ref, f"paged prefill {page_size}")
+    np.testing.assert_allclose(lse.cpu().numpy(), l_ref, rtol=1e-5, atol=1e-5)
+    assert dsa.device_status() == 0
+
+
 @pytest.mark.parametrize("slices", [1, 3])
 def test_host_prefill_matches_device_calls(dsa, slices):
     """HostPrefill (pinned host in, pinned host out, copies overlapped) gives the same bits as the
