@@ -451,6 +451,8 @@ def run_gpu(args, wl, rank, world, local_rank):
         "data": "synthetic",
         "config": config_block(wl, world),
         "roofline": roof,
+        # indexer + top-k per chunk (the selection stage on its own)
+        "indexer_topk_ms": float(kern_ms[0] + kern_ms[1]),
         "kernels_ms": {"dsa_indexer_scores": float(kern_ms[0]), "dsa_topk": float(kern_ms[1]),
                        attn_name: float(kern_ms[2])},
         "kernel_rooflines": {
