@@ -69,6 +69,7 @@ constexpr int kWorkerWarps = 16;                  // gather + softmax warps
 constexpr int kWorkers = kWorkerWarps * 32;        // 512
 constexpr int kThreads = 64 + kWorkers;            // warp 0 Q loader, warp 1 MMA, warps 2.. workers
 constexpr int kHG = kH / (kWorkerWarps / 4);       // 16 heads per worker warp
+constexpr int kGroupThreads = 4 * 32;              // the four warps sharing a head group
 constexpr int kSegs = 4;               // PV releases the stage by 128-dim latent chunk (the rope block with the last)
 static_assert(kWorkerWarps == 16 && kTile == 128, "a worker warp copies four rows of each 64-key half");
 constexpr float kRescaleThreshold = 16.0f;  // log2 units
@@ -327,6 +328,8 @@ __global__ void __launch_bounds__(kThreads, 1)   // 18 warps: at most 96 registe
         const int quad = warp & 3;                // TMEM lane quadrant this warp may access
         const int hg = ww >> 2;                   // head group: heads h0 .. h0 + 15
         const int h0 = hg * kHG;
+        // the head group's four warps (one per TMEM lane quadrant) agree on rescaling among themselves
+        const uint32_t group_bar = 3 + (uint32_t)hg;
         const int tid = ww * 32 + (int)lane;      // 0..511
         const int key = quad * 32 + (int)lane;    // TMEM lane == key row of the tile == dim row of O^T
         const uint32_t lane_addr = static_cast<uint32_t>(quad * 32) << 16;
@@ -486,27 +489,27 @@ __global__ void __launch_bounds__(kThreads, 1)   // 18 warps: at most 96 registe
                         viol |= x[4 * h4 + 2] * p.scale_log2 > m4.z + kRescaleThreshold;
                         viol |= x[4 * h4 + 3] * p.scale_log2 > m4.w + kRescaleThreshold;
                     }
-                    need_red = named_bar_or(1, kWorkers, viol);
+                    need_red = named_bar_or(group_bar, kGroupThreads, viol);
                 }
                 bool any_upd = false;
                 if (need_red) {
                     const float r = warp_transpose_reduce16<true>(x, lane);
                     if ((lane & 1u) == 0) red[quad * kH + h0 + (int)(lane >> 1)] = r;
-                    named_bar_sync(1, kWorkers);
+                    named_bar_sync(group_bar, kGroupThreads);
                     bool upd = false;
-                    if (tid < kH) {
-                        const float mt = p.scale_log2 * fmaxf(fmaxf(red[tid], red[kH + tid]),
-                                                              fmaxf(red[2 * kH + tid], red[3 * kH + tid]));
-                        const float mo = m_used[tid];
+                    if (ww == 4 * hg && lane < kHG) {   // one lane per head of the group
+                        const int h = h0 + (int)lane;
+                        const float mt = p.scale_log2 * fmaxf(fmaxf(red[h], red[kH + h]), fmaxf(red[2 * kH + h], red[3 * kH + h]));
+                        const float mo = m_used[h];
                         float a = 1.f;
                         if (mt > -INFINITY && (mo == -INFINITY || mt > mo + kRescaleThreshold)) {
                             a = (mo == -INFINITY) ? 0.f : ex2_approx(mo - mt);
-                            m_used[tid] = mt;
+                            m_used[h] = mt;
                             upd = (mo != -INFINITY);
                         }
-                        alpha_s[tid] = a;
+                        alpha_s[h] = a;
                     }
-                    any_upd = named_bar_or(1, kWorkers, upd);
+                    any_upd = named_bar_or(group_bar, kGroupThreads, upd);
                 }
                 // probabilities (bf16 for the MMA, float32 for the row sum)
                 uint32_t packed[kHG / 2];
