@@ -36,7 +36,9 @@
 //     thread.  Each head's reference maximum is taken from the query's first
 //     tile (transposing warp butterfly + one shared-memory exchange); later
 //     tiles only check, per thread, whether a score exceeds its reference by
-//     more than 2^16, and only then reduce and rescale O^T in TMEM.
+//     more than 2^16, and only then reduce and rescale O^T in TMEM; the vote,
+//     the reduction and the new references involve only the four warps (one
+//     per lane quadrant) that share a group of 16 heads.
 //     Numerator and denominator always share the reference, so the result is
 //     the exact softmax.  P^T is written as bf16 into the (consumed) rope
 //     block.
