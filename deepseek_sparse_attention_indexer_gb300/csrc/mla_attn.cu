@@ -27,11 +27,15 @@
 //     block too), so the next tile's copies of a chunk, and then its QK
 //     segment, overlap the rest of PV (measured against releasing 64-key
 //     halves: 1.93 -> 1.91 ms at 16k keys, 2.09 -> 1.91 ms at 64k keys).
-//     The copies of tile t+1 are issued right after
-//     the warp's softmax of tile t, so the whole CTA issues copies (cp.async
-//     throughput from L2 grows with the number of issuing warps).  QK waits
-//     per 128-dim chunk of the K-dim.  Unselected or padding slots are
-//     zero-filled.
+//     The copies of tile t+1 are issued right after the warp's softmax of
+//     tile t, so the whole CTA issues copies (cp.async throughput from L2
+//     grows with the number of issuing warps).  QK waits per 128-dim chunk of
+//     the K-dim.  Unselected or padding slots are zero-filled.  (Timing
+//     variants without any copies ran as fast: the MMA stream and the softmax
+//     between QK and PV bound a tile, and one 144 KB stage plus the 72 KB
+//     Q^T leave no room for a second tile or query to overlap them.)
+//   * Paged caches (PAGED): a row's cache address comes from the sequence's
+//     page table, looked up after the index load.
 //   * Softmax: four warps per TMEM lane quadrant, 16 heads each, one key per
 //     thread.  Each head's reference maximum is taken from the query's first
 //     tile (transposing warp butterfly + one shared-memory exchange); later
