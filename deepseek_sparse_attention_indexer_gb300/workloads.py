@@ -13,6 +13,8 @@ Shapes follow the GLM-5.x / DeepSeek sparse-attention layer traced on the pages
 * head weights   w   [B, L, 32]       f32
 * absorbed query q   [B, L, 64, 576]  bf16 ([q_nope.wk_b 512 | q_pe 64])
 * latent KV row  kv  [B, N, 576]      bf16 ([kv_cmpr 512 | k_pe 64])
+* attention out  o   [R, 64, 512]     bf16 (input of the value up-projection)
+* value weights  wv  [64, 256, 512]   bf16 (wv_b: one 512-wide row per value feature)
 
 Value recipes (fixed per workload, seeded):
 
@@ -23,6 +25,8 @@ Value recipes (fixed per workload, seeded):
   [-8, 8] times 2^-4.  Every indexer product and head sum is then an exact
   multiple of 2^-10 far inside float32's 24-bit mantissa, so float32 scores
   are exact and the top-k sets are unique under the lower-index tie rule.
+* o: standard normal rounded to bf16; wv: standard normal times 2^-5 rounded
+  to bf16 (so each 512-term value sum has standard deviation about 0.7).
 * The 64k workload copies indexer-key rows onto 5% of the keys (distinct
   seeded targets, seeded sources), so those keys score exactly like another
   key for every query that sees both: a tie stress for the top-2048 boundary.
@@ -42,6 +46,7 @@ IDX_DIM = 128         # indexer head dim
 N_HEADS = 64          # attention query heads
 QK_DIM = 576          # kv_lora_rank 512 + qk_rope_head_dim 64
 V_DIM = 512           # kv_lora_rank
+V_HEAD_DIM = 256      # v_head_dim (value width per head after the wv_b up-projection)
 SCALE = 1.0 / 16.0    # 1/sqrt(qk_nope_head_dim 192 + qk_rope_head_dim 64)
 
 
@@ -143,6 +148,15 @@ def make_attention_inputs(wl: Workload, seed: Optional[int] = None):
         kv32[..., V_DIM:] *= np.float32(wl.rope_std)
     kv = f32_to_bf16_bits(kv32)
     return q, kv
+
+
+def make_value_proj_inputs(R: int, seed: int):
+    """o [R, 64, 512] bf16 bits (attention-output stand-in) and wv [64, 256, 512] bf16 bits."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    o = f32_to_bf16_bits(rng.standard_normal((R, N_HEADS, V_DIM), dtype=np.float32))
+    wv = f32_to_bf16_bits(rng.standard_normal((N_HEADS, V_HEAD_DIM, V_DIM), dtype=np.float32)
+                          * np.float32(2.0 ** -5))
+    return o, wv
 
 
 def positions(wl: Workload):

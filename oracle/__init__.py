@@ -51,7 +51,8 @@ def _load():
             lib.oracle_topk.argtypes = [P, ctypes.c_int64, P, P, I, I, I, I, I, P]
             lib.oracle_attn.argtypes = [P, P, P, P, I, I, I, I, I, ctypes.c_double,
                                         I, I, P, P]
-            for f in (lib.oracle_indexer, lib.oracle_topk, lib.oracle_attn):
+            lib.oracle_value_up_proj.argtypes = [P, P, I, I, I, I, I, P]
+            for f in (lib.oracle_indexer, lib.oracle_topk, lib.oracle_attn, lib.oracle_value_up_proj):
                 f.restype = None
             _lib = lib
     return _lib
@@ -164,6 +165,28 @@ def attention(q: np.ndarray, kv: np.ndarray, idx: np.ndarray, row_batch: np.ndar
                         Dv, float(scale), b, e, _ptr(out) + k * H * Dv * 8, _ptr(lse) + k * H * 8)
     _run(fn, _split(rows, threads), threads)
     return out, lse
+
+
+def value_up_proj(o: np.ndarray, wv: np.ndarray, rows: Optional[Sequence[int]] = None,
+                  threads: int = 1) -> np.ndarray:
+    """v [R, H, E] float64 = per head o[r, h, :] . wv[h, e, :] (the wv_b up-projection).
+
+    o [R, H, Dv] bf16 bits, wv [H, E, Dv] bf16 bits.  With `rows`, v holds only
+    those (sorted) rows.
+    """
+    lib = _load()
+    R, H, Dv = o.shape
+    H2, E, Dv2 = wv.shape
+    assert H2 == H and Dv2 == Dv
+    o = np.ascontiguousarray(o, np.uint16)
+    wv = np.ascontiguousarray(wv, np.uint16)
+    rows = list(range(R)) if rows is None else sorted(rows)
+    v = np.full((len(rows), H, E), np.nan, dtype=np.float64)
+
+    def fn(b, e, k):
+        lib.oracle_value_up_proj(_ptr(o), _ptr(wv), H, Dv, E, b, e, _ptr(v) + k * H * E * 8)
+    _run(fn, _split(rows, threads), threads)
+    return v
 
 
 def unpage(pool: np.ndarray, block_table: np.ndarray, page_size: int, kv_len,

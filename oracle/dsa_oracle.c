@@ -197,3 +197,32 @@ void oracle_attn(const uint16_t *q, const uint16_t *kv, const int32_t *idx,
     }
     free(s);
 }
+
+/*
+ * Value up-projection (wv_b) of the attention output, per head.
+ *   v[r, h, e] = sum_{d < Dv} o[r, h, d] * wv[h, e, d]      for e < E
+ * SlimServe "GLM52_PIPELINE_TRACE.md", section 6 "Attention core (absorbed
+ * MLA)": the product with wv_b decompresses each head's latent output (width
+ * kv_lora_rank 512 = Dv) into its value (v_head_dim 256 = E, Config line).
+ * The weight layout (one Dv-wide row per value feature, per head) is the
+ * library's reading; the pages fix only the shapes.
+ *   o [R, H, Dv] is indexed by absolute row; wv [H, E, Dv];
+ *   v [row_end - row_begin, H, E] starts at row row_begin.
+ */
+void oracle_value_up_proj(const uint16_t *o, const uint16_t *wv, int H, int Dv, int E,
+                          int row_begin, int row_end, double *v)
+{
+    for (int r = row_begin; r < row_end; ++r) {
+        for (int h = 0; h < H; ++h) {
+            const uint16_t *orow = o + ((size_t)r * H + h) * Dv;
+            double *vr = v + ((size_t)(r - row_begin) * H + h) * E;
+            for (int e = 0; e < E; ++e) {
+                const uint16_t *wr = wv + ((size_t)h * E + e) * Dv;
+                double acc = 0.0;
+                for (int d = 0; d < Dv; ++d)
+                    acc += bf16_to_double(orow[d]) * bf16_to_double(wr[d]);
+                vr[e] = acc;
+            }
+        }
+    }
+}

@@ -8,7 +8,10 @@ mathematics fix, none of which reuses the oracle's own code.
   the "query before position top_k keeps every earlier key" rule;
 * attention: closed form on two keys, dense causal softmax attention (scipy)
   whenever top_k covers every causal key, one-key and zero-query cases,
-  invariance to the order of the selected indices.
+  invariance to the order of the selected indices;
+* value up-projection: permutation weights (pure selection), prefix-sum
+  weights (numpy cumsum), independence of heads and rows;
+* indexer layer schedule: the pages' 8-layer example and its structure.
 """
 import itertools
 import json
@@ -305,3 +308,94 @@ def test_paginate_then_unpage_is_identity(oracle_mod):
         for b, n in enumerate(kv_len):
             np.testing.assert_array_equal(back[b, :n], dense[b, :n])
             assert not back[b, n:].any()
+
+
+# ----------------------------------------------------------------------------- value up-projection
+
+def _bf16_f64(bits):
+    return W.bf16_bits_to_f32(bits).astype(np.float64)
+
+
+def test_value_up_proj_permutation_weights(oracle_mod):
+    """wv[h, e, d] = 1 exactly when d = sigma_h(e) (a different permutation per head): the
+    projection only selects, v[r, h, e] = o[r, h, sigma_h(e)].  A transposed weight, a
+    wrong head or a dropped term changes the result."""
+    rng = np.random.default_rng(11)
+    R, H, Dv, E = 5, 3, 24, 10
+    o = _bf(rng.standard_normal((R, H, Dv)))
+    sig = np.stack([rng.permutation(Dv)[:E] for _ in range(H)])
+    wv = np.zeros((H, E, Dv), np.float32)
+    for h in range(H):
+        wv[h, np.arange(E), sig[h]] = 1.0
+    v = oracle_mod.value_up_proj(o, _bf(wv))
+    of = _bf16_f64(o)
+    expect = np.stack([of[:, h, sig[h]] for h in range(H)], axis=1)
+    np.testing.assert_array_equal(v, expect)
+
+
+def test_value_up_proj_prefix_sum_weights(oracle_mod):
+    """wv[h, e, d] = c_h for d <= e, else 0, with c_h a power of two: v[r, h, e] is c_h times
+    the prefix sum of the head's latent row up to e (numpy cumsum; exact in float64 for
+    bf16 inputs of this range)."""
+    rng = np.random.default_rng(12)
+    R, H, Dv, E = 4, 4, 64, 64
+    o = _bf(rng.standard_normal((R, H, Dv)))
+    c = np.array([1.0, 0.5, 2.0, 0.25], np.float32)
+    tri = np.tril(np.ones((E, Dv), np.float32))          # row e: ones at d <= e
+    wv = c[:, None, None] * tri[None]
+    v = oracle_mod.value_up_proj(o, _bf(wv))
+    expect = np.cumsum(_bf16_f64(o), axis=2) * c.astype(np.float64)[None, :, None]
+    np.testing.assert_array_equal(v, expect)
+
+
+def test_value_up_proj_heads_are_independent(oracle_mod):
+    """Zeroing every head's weights but one zeroes every other head's output and leaves that
+    head's output as it was; the rows are independent too (a row subset gives the same rows)."""
+    R, H = 6, 64
+    o, wv = W.make_value_proj_inputs(R, seed=13)
+    o, wv = o[:, :, :], wv[:, :32, :]                     # E = 32 keeps the pin fast
+    full = oracle_mod.value_up_proj(o, wv)
+    only = np.zeros_like(wv)
+    only[17] = wv[17]
+    v = oracle_mod.value_up_proj(o, only)
+    assert not np.delete(v, 17, axis=1).any()
+    np.testing.assert_array_equal(v[:, 17], full[:, 17])
+    sub = oracle_mod.value_up_proj(o, wv, rows=[1, 4, 5])
+    np.testing.assert_array_equal(sub, full[[1, 4, 5]])
+
+
+# ----------------------------------------------------------------------------- indexer layer schedule
+
+def test_indexer_schedule_matches_the_pages_example():
+    """The first 8 GLM-5.3 layers (index_topk_freq 4, index_skip_topk_offset 3): layers
+    0, 1, 2 and 6 run the indexer, 3, 4, 5 and 7 reuse a selection (worked example printed
+    on the exo page; stored under tests/golden with its citation)."""
+    from deepseek_sparse_attention_indexer_gb300 import _build, _lib
+    _build.build()
+    g = json.load(open(os.path.join(GOLDEN, "indexer_layer_schedule.json")))
+    f, off = g["index_topk_freq"], g["index_skip_topk_offset"]
+    for layer in g["indexer_layers"]:
+        assert _lib.indexer_source_layer(layer, f, off) == layer
+    for layer in g["shared_layers"]:
+        assert _lib.indexer_source_layer(layer, f, off) != layer
+
+
+@pytest.mark.parametrize("freq,off", [(4, 3), (1, 1), (2, 5), (3, 1)])
+def test_indexer_schedule_reuses_the_nearest_indexer_layer(freq, off):
+    """Every shared layer reuses the nearest earlier layer that ran the indexer, and runs of
+    shared layers between two indexer layers are freq - 1 long after the offset."""
+    from deepseek_sparse_attention_indexer_gb300 import _build, _lib
+    _build.build()
+    src = [_lib.indexer_source_layer(layer, freq, off) for layer in range(40)]
+    runs = [layer for layer in range(40) if src[layer] == layer]
+    assert runs[:off] == list(range(off))
+    for layer in range(40):
+        if src[layer] != layer:
+            assert src[layer] < layer and src[src[layer]] == src[layer]
+            assert not any(src[m] == m for m in range(src[layer] + 1, layer))
+    after = [layer for layer in runs if layer >= off]
+    assert all(b - a == freq for a, b in zip(after, after[1:]))
+    assert not after or after[0] == off + freq - 1
+    for bad in [(-1, freq, off), (0, 0, off), (0, freq, 0)]:
+        with pytest.raises(ValueError):
+            _lib.indexer_source_layer(*bad)
