@@ -100,6 +100,18 @@ def attention_traffic(wl, decode):
     return None
 
 
+def value_proj_line(R, ms, peaks, peak_kind):
+    """Roofline of one mla_value_up_proj launch over R rows (bound by HBM: o in, v out)."""
+    nbytes = R * 64 * 512 * 2 + 64 * 256 * 512 * 2 + R * 64 * 256 * 2
+    flop = R * 64 * 256 * 512 * 2
+    hbm = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    tf = flop / (ms * 1e-3) / 1e12
+    return {"rows": R, "ms": ms, "bound": "hbm", "achieved_gbs": gbs, "frac": gbs / hbm,
+            "peak_kind": f"{peak_kind} HBM copy", "bytes_per_launch": nbytes, "tflops": tf,
+            "note": "wv_b up-projection of the step's attention output, timed after the step (not in the metric)"}
+
+
 def load_peaks():
     try:
         with open(PEAKS_PATH) as f:
@@ -408,6 +420,26 @@ def run_gpu(args, wl, rank, world, local_rank):
         e2e_ms.append(e0.elapsed_time(e1))
     e2e_mean = max_over_ranks(float(np.mean(e2e_ms)), world, dev)
 
+    # ---- the value up-projection (wv_b) of this step's attention output: the layer's next
+    # call after the path, timed on its own (not part of the metric); L2 flushed before each call
+    R_v = out.shape[0]
+    _, wv_host = W.make_value_proj_inputs(1, seed=wl.seed + 31)
+    dwv = d(wv_host)
+    vout = torch.empty((R_v, 64, 256), dtype=torch.bfloat16, device=dev)
+    for _ in range(3):
+        dsa.mla_value_up_proj(out, dwv, v=vout)
+    vp_ms = []
+    for _ in range(max(3, min(args.steps, 20))):
+        flush.zero_()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        dsa.mla_value_up_proj(out, dwv, v=vout)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        vp_ms.append(e0.elapsed_time(e1))
+    vp_ms = float(np.mean(vp_ms))
+
     if rank != 0:
         return 0
 
@@ -466,6 +498,7 @@ def run_gpu(args, wl, rank, world, local_rank):
         "graph": ({"ms_per_step": graph_ms, "note": "the step replayed as one CUDA graph, inputs resident, "
                    "no L2 flush between replays"} if isinstance(graph_ms, float) else {"ms_per_step": None,
                                                                                      "note": graph_ms}),
+        "value_up_proj": value_proj_line(R_v, vp_ms, peaks, peak_kind),
         "gpu_launches": (4 if decode else 3) * args.steps,
         "clocks": clocks,
         "device_status": status,

@@ -44,6 +44,8 @@ SIGNATURES = {
     "mla_sparse_attn_decode_paged": (ctypes.c_int32, [_P, _P, _P, _P, _I, _I, _I, _P, _I, _I, _I, _F, _P, _P, _P,
                                                       _SZ, _P]),
     "mla_sparse_attn_prefill_paged": (ctypes.c_int32, [_P, _P, _P, _I, _I, _P, _I, _I, _I, _F, _P, _P, _P, _SZ, _P]),
+    "mla_value_up_proj": (ctypes.c_int32, [_P, _P, _I, _P, _P]),
+    "dsa_indexer_source_layer": (ctypes.c_int, [_I, _I, _I]),
     "dsa_device_status": (ctypes.c_int32, [_P, ctypes.POINTER(ctypes.c_int32), _I]),
 }
 
@@ -264,6 +266,29 @@ def mla_sparse_attn_prefill_paged(q: torch.Tensor, kv_pool: torch.Tensor, block_
                                               _stream(stream))
     _check("mla_sparse_attn_prefill_paged", rc)
     return (out, lse) if want_lse else out
+
+
+def mla_value_up_proj(o: torch.Tensor, wv_b: torch.Tensor, v: Optional[torch.Tensor] = None,
+                      stream=None) -> torch.Tensor:
+    """v [R, 64, 256] bf16 = per head o[r, h, :] (512 latent dims) times wv_b[h]^T,
+    for o [R, 64, 512] and wv_b [64, 256, 512] (bf16)."""
+    R = o.shape[0]
+    assert _is16(o) and _is16(wv_b)
+    assert tuple(o.shape[1:]) == (64, 512) and tuple(wv_b.shape) == (64, 256, 512)
+    if v is None:
+        v = torch.empty((R, 64, 256), dtype=torch.bfloat16, device=o.device)
+    rc = load().mla_value_up_proj(_ptr(o), _ptr(wv_b), R, _ptr(v), _stream(stream))
+    _check("mla_value_up_proj", rc)
+    return v
+
+
+def indexer_source_layer(layer: int, topk_freq: int = 4, skip_offset: int = 3) -> int:
+    """The layer whose top-k selection `layer` attends with (itself if it runs the
+    indexer); GLM-5.x shares the indexer with index_topk_freq 4, index_skip_topk_offset 3."""
+    r = load().dsa_indexer_source_layer(layer, topk_freq, skip_offset)
+    if r < 0:
+        raise ValueError(f"invalid layer schedule arguments ({layer}, {topk_freq}, {skip_offset})")
+    return r
 
 
 def device_status(reset: bool = True, stream=None) -> int:

@@ -301,6 +301,24 @@ dsa_status_t mla_sparse_attn_decode_noalloc(const void* q, const void* kv, const
                                       static_cast<cudaStream_t>(stream));
 }
 
+dsa_status_t mla_value_up_proj(const void* o, const void* wv_b, int R, void* v, void* stream) {
+    if (!o || !wv_b || !v) return DSA_ERR_INVALID_ARG;
+    if (R < 1) return DSA_ERR_INVALID_ARG;
+    if ((long long)R * DSA_HEADS > 0x7FFFFFFFLL) return DSA_ERR_UNSUPPORTED_SHAPE;
+    if (!aligned16(o) || !aligned16(wv_b) || !aligned16(v)) return DSA_ERR_MISALIGNED;
+    dsa_status_t st = check_device();
+    if (st != DSA_OK) return st;
+    return launch_value_up_proj(o, wv_b, R, v, static_cast<cudaStream_t>(stream));
+}
+
+int dsa_indexer_source_layer(int layer, int topk_freq, int skip_offset) {
+    if (layer < 0 || topk_freq < 1 || skip_offset < 1) return -1;
+    if (layer < skip_offset) return layer;
+    // layers skip_offset + topk_freq - 1, + 2 topk_freq - 1, ... run the indexer
+    const int k = (int)(((long long)layer - skip_offset + 1) % topk_freq);
+    return layer - k;
+}
+
 dsa_status_t dsa_device_status(void* stream, int32_t* code_out, int reset) {
     if (!code_out) return DSA_ERR_INVALID_ARG;
     cudaStream_t s = static_cast<cudaStream_t>(stream);

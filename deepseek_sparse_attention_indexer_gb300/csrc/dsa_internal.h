@@ -76,5 +76,6 @@ dsa_status_t launch_attn_decode_noalloc(const void* q, const void* kv, const int
 dsa_status_t launch_attn_decode(const void* q, const void* kv, const int32_t* kv_len, const int32_t* idx, int B,
                                 int Nmax, int top_k, float scale, void* out, float* lse, void* workspace,
                                 const PageTable& pages, cudaStream_t stream);
+dsa_status_t launch_value_up_proj(const void* o, const void* wv_b, int R, void* v, cudaStream_t stream);
 
 }  // namespace dsa

@@ -20,7 +20,8 @@
  *   - The model constants are fixed to the GLM-5.x layer traced on the pages
  *     (SlimServe "GLM52_PIPELINE_TRACE.md", Config line; exo PR #2539,
  *     section Prefill): 32 indexer heads of width 128, 64 attention heads,
- *     576-wide absorbed query/key ([512 latent | 64 rope]), 512-wide latent V.
+ *     576-wide absorbed query/key ([512 latent | 64 rope]), 512-wide latent V,
+ *     256-wide per-head value after the wv_b up-projection.
  *     Other shapes are DSA_ERR_UNSUPPORTED_SHAPE: there is no fallback path.
  */
 #ifndef DSA_GB300_H
@@ -33,13 +34,14 @@
 extern "C" {
 #endif
 
-#define DSA_ABI_VERSION 2  /* 2: paged-cache entry points */
+#define DSA_ABI_VERSION 3  /* 2: paged-cache entry points; 3: value up-projection, indexer layer schedule */
 
 #define DSA_INDEXER_HEADS 32
 #define DSA_INDEXER_DIM 128
 #define DSA_HEADS 64
 #define DSA_QK_DIM 576
 #define DSA_V_DIM 512
+#define DSA_V_HEAD_DIM 256
 #define DSA_MAX_TOPK 2048
 
 typedef int32_t dsa_status_t;
@@ -236,6 +238,44 @@ dsa_status_t mla_sparse_attn_prefill_paged(const void *q, const void *kv_pool,
                                            const int32_t *idx, int L, int N, int top_k, float scale,
                                            void *out, float *lse, void *workspace, size_t ws_bytes,
                                            void *stream);
+
+/*
+ * mla_value_up_proj -- the value up-projection (wv_b) after the attention.
+ * Defined on SlimServe "GLM52_PIPELINE_TRACE.md", section 6 "Attention core
+ * (absorbed MLA)": the attention's output lives in the 512-wide latent space
+ * and the product with wv_b decompresses it to each head's value ("MQA ->
+ * MHA"); Config line: kv_lora_rank 512, v_head_dim 256, 64 heads.  exo PR
+ * #2539, section "Prefill": the value up-projection runs once for all queries.
+ *
+ *   v[r, h, e] = sum_{d<512} o[r, h, d] * wv_b[h, e, d]     for e < 256
+ *
+ *   o     bf16 [R, 64, 512]    attention output (mla_sparse_attn_prefill / _decode)
+ *   wv_b  bf16 [64, 256, 512]  per head, one 512-wide row per value feature
+ *                              (the row-major layout of a per-head [256 x 512] weight)
+ *   v     bf16 [R, 64, 256]    output (round to nearest even from float32)
+ * bf16 x bf16 products accumulated in float32 by the tensor cores.  R >= 1 rows
+ * (a prefill chunk's queries, or one row per sequence in decode).  All three
+ * pointers 16-byte aligned.  Needs no workspace.
+ */
+dsa_status_t mla_value_up_proj(const void *o, const void *wv_b, int R, void *v, void *stream);
+
+/*
+ * dsa_indexer_source_layer -- which layer's top-k selection a layer attends
+ * with, when the indexer is shared across layers.
+ * SlimServe "GLM52_PIPELINE_TRACE.md", Config line: index_topk_freq and
+ * index_skip_topk_offset (4 and 3 for GLM-5.x); exo PR #2539, section
+ * "Correctness" (weights bullet): of the first 8 layers, layers 0, 1, 2 and 6
+ * run the indexer and layers 3, 4, 5 and 7 reuse a selection.  Reading (the
+ * pages give only these values and that example): every layer below
+ * skip_offset runs the indexer; from skip_offset on, layer l runs it when
+ * (l - skip_offset + 1) is a multiple of topk_freq, and otherwise reuses the
+ * selection of the nearest earlier layer that ran it.
+ *
+ * Returns `layer` itself when the layer runs the indexer, the earlier layer it
+ * reuses otherwise, or -1 for invalid arguments (layer < 0, topk_freq < 1,
+ * skip_offset < 1).  Host-only, pure function.
+ */
+int dsa_indexer_source_layer(int layer, int topk_freq, int skip_offset);
 
 /*
  * dsa_device_status -- synchronise `stream`, then read (and if `reset` is

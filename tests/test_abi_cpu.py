@@ -32,7 +32,7 @@ def test_header_declares_the_path():
     for n in ["dsa_indexer_scores", "dsa_topk", "mla_sparse_attn_prefill", "mla_sparse_attn_decode",
               "dsa_status_string", "dsa_abi_version", "dsa_device_status", "dsa_topk_workspace_size",
               "mla_sparse_attn_workspace_size", "dsa_indexer_scores_paged", "mla_sparse_attn_decode_paged",
-              "mla_sparse_attn_prefill_paged"]:
+              "mla_sparse_attn_prefill_paged", "mla_value_up_proj", "dsa_indexer_source_layer"]:
         assert n in names
 
 
@@ -48,7 +48,7 @@ def test_exports_every_declared_symbol(lib):
 
 
 def test_version_and_strings(lib):
-    assert lib.dsa_abi_version() == 2
+    assert lib.dsa_abi_version() == 3
     for code in range(0, 10):
         s = lib.dsa_status_string(code)
         assert s and len(s) > 1
@@ -96,6 +96,12 @@ def test_host_validation_rejects_bad_arguments(lib):
     assert pre_paged(P, P, P, 48, 8, P, 4, 256, 32, 0.0625, P, None, None, 0, stream) == 2         # page size
     assert pre_paged(P, P, P, 64, 8, P, 4, 256, 4096, 0.0625, P, None, None, 0, stream) == 2       # top_k
     assert pre_paged(P, P + 4, P, 64, 8, P, 4, 256, 32, 0.0625, P, None, None, 0, stream) == 3     # kv_pool
+    # value up-projection
+    assert lib.mla_value_up_proj(None, P, 4, P, stream) == 1
+    assert lib.mla_value_up_proj(P, P, 0, P, stream) == 1
+    assert lib.mla_value_up_proj(P, P, 1 << 30, P, stream) == 2                    # R * 64 > 2^31 - 1
+    assert lib.mla_value_up_proj(P, P + 8, 4, P, stream) == 3
+    assert lib.mla_value_up_proj(P, P, 4, P + 2, stream) == 3
     code = ctypes.c_int32(0)
     assert lib.dsa_device_status(None, None, 0) == 1
 
