@@ -305,7 +305,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 float* srow = srow_item + t * kTileKeys;
                 if (t < I.n_comp_end) {
                     const int acc = acc_it % C::NACC;
-                    if (!(ok = mbar_wait(&acc_full[acc], (acc_it / C::NACC) & 1, abort_flag, p.status))) break;
+                    // warp-uniform outcome: the TMEM load below is warp-collective
+                    ok = __all_sync(0xffffffffu, mbar_wait(&acc_full[acc], (acc_it / C::NACC) & 1, abort_flag, p.status));
+                    if (!ok) break;
                     tc_fence_after();
                     if (q < QG) {   // warp-uniform: TMEM columns of this query exist
                         uint32_t v[32];
