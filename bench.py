@@ -388,8 +388,9 @@ def run_gpu(args, wl, rank, world, local_rank):
     if not decode and wl.B == 1:
         # the package's host-buffer prefill: copies on side streams overlap the kernels
         from deepseek_sparse_attention_indexer_gb300.host_prefill import HostPrefill
-        runner = HostPrefill(wl.L, wl.N, wl.top_k, device=dev, slices=4)
-        e2e_api = "HostPrefill: H2D of the inputs, the three calls and D2H of the output overlapped (4 query slices)"
+        runner = HostPrefill(wl.L, wl.N, wl.top_k, device=dev)
+        e2e_api = (f"HostPrefill: H2D of the inputs, the three calls and D2H of the output overlapped "
+                   f"({runner.slices} query slices)")
 
         def e2e_step():
             runner(*host_in, host_out, W.SCALE, stream=stream)

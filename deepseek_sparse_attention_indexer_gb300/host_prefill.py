@@ -11,10 +11,15 @@ copies around them so that they overlap the kernels:
 Attention runs per slice of the chunk's queries (each slice is one
 `mla_sparse_attn_prefill` call over its rows of q, idx and out), so a slice
 starts as soon as its part of q has landed and its output is copied back while
-the next slice computes.  Every step of the method still runs in the library's
-kernels; nothing here computes.
+the next slice computes.  By default a slice is two rounds of the attention's
+persistent CTAs (2 x the SM count queries): the device->host copy of a slice
+(about 0.11 ms for 304 queries) then keeps pace with the attention, and only
+the last slice's copy trails the compute.  Every step of the method still runs
+in the library's kernels; nothing here computes.
 """
 from __future__ import annotations
+
+from typing import Optional
 
 import torch
 
@@ -30,9 +35,12 @@ class HostPrefill:
     for the copies to be asynchronous.
     """
 
-    def __init__(self, L: int, N: int, top_k: int, device=None, slices: int = 4):
+    def __init__(self, L: int, N: int, top_k: int, device=None, slices: Optional[int] = None):
         self.L, self.N, self.top_k = L, N, top_k
         self.dev = torch.device(device if device is not None else "cuda")
+        if slices is None:   # two rounds of one attention CTA per SM a slice
+            per_slice = 2 * torch.cuda.get_device_properties(self.dev).multi_processor_count
+            slices = (L + per_slice - 1) // per_slice
         self.slices = max(1, min(slices, L))
         dev = self.dev
         self.d_qi = torch.empty((1, L, 32, 128), dtype=torch.int16, device=dev)
