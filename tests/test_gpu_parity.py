@@ -445,12 +445,13 @@ def test_paged_chunked_prefill_chain(dsa, oracle_mod, page_size):
     assert dsa.device_status() == 0
 
 
-@pytest.mark.parametrize("slices", [1, 3])
-def test_host_prefill_matches_device_calls(dsa, slices):
+@pytest.mark.parametrize("L,slices", [(77, 1), (77, 3), (700, None)])
+def test_host_prefill_matches_device_calls(dsa, L, slices):
     """HostPrefill (pinned host in, pinned host out, copies overlapped) gives the same bits as the
-    three device calls on device copies of the same inputs."""
+    three device calls on device copies of the same inputs; slices=None is the default split into
+    slices of two rounds of attention CTAs (three slices of at most 304 queries here)."""
     from deepseek_sparse_attention_indexer_gb300.host_prefill import HostPrefill
-    wl = W.custom("host_ragged", B=1, L=77, p0=1100, N=1177, top_k=256, seed=51)
+    wl = W.custom("host_ragged", B=1, L=L, p0=1100, N=1100 + L, top_k=256, seed=51)
     qi, ki, w = W.make_indexer_inputs(wl)
     q, kv = W.make_attention_inputs(wl)
     q_pos0, kv_len = W.positions(wl)
@@ -458,6 +459,8 @@ def test_host_prefill_matches_device_calls(dsa, slices):
     h = [pin(a) for a in (qi, ki, w, q_pos0, kv_len, q, kv)]
     h_out = torch.empty((wl.L, 64, 512), dtype=torch.bfloat16).pin_memory()
     runner = HostPrefill(wl.L, wl.N, wl.top_k, slices=slices)
+    if slices is None:
+        assert runner.slices == -(-L // (2 * torch.cuda.get_device_properties(0).multi_processor_count))
     for _ in range(2):                  # the buffers are reused across calls
         runner(*h, h_out, W.SCALE)
         torch.cuda.synchronize()
