@@ -130,6 +130,24 @@ def test_topk_bit_exact_with_ties(dsa, oracle_mod, rows, n, K, p0):
     np.testing.assert_array_equal(idx.cpu().numpy()[0], ref)
 
 
+@pytest.mark.parametrize("rows,n", [(12, 50000), (4, 65536), (3, 65537)])
+def test_topk_long_rows_continuous_scores(dsa, oracle_mod, rows, n):
+    """Rows over 16384 keys with a small threshold bucket take the candidate-list path (the
+    keys at or above the threshold bucket copied in index order into shared memory), at, below
+    and one past 65536 keys."""
+    S = W.random_scores(rows, n, seed=n + rows, ties=False)
+    K = 2048
+    q_pos0 = np.array([n - rows], np.int32)
+    kv_len = np.array([n], np.int32)
+    ld = (n + 3) // 4 * 4
+    Sp = np.full((1, rows, ld), np.nan, np.float32)
+    Sp[0, :, :n] = S
+    idx = dsa.topk(dev(Sp), dev(q_pos0), dev(kv_len), n, K)
+    torch.cuda.synchronize()
+    ref = oracle_mod.topk(S, q_pos0, kv_len, 1, rows, K)
+    np.testing.assert_array_equal(idx.cpu().numpy()[0], ref)
+
+
 @pytest.mark.parametrize("n_tied", [2500, 2584, 2585, 2600])
 def test_topk_long_rows_tie_block_at_list_capacity(dsa, oracle_mod, n_tied):
     """Rows longer than 16384 keys: 1000 keys above a block of n_tied equal keys that holds the
