@@ -25,7 +25,10 @@
 //     bound, and more rows in flight win for short rows, while long rows do
 //     not fit in registers.  For long rows a thread keeps four float4 loads in
 //     flight per histogram step and compacts a run of eight float4 per block
-//     scan (64k keys: 0.90 -> 0.69 ms for 4096 rows on GB300).
+//     scan (64k keys: 0.90 -> 0.69 ms for 4096 rows on GB300).  Rows of at least
+//     32768 keys first take a lower bound for the threshold bucket from an
+//     eighth of the row and copy every key above it into a shared-memory list
+//     in one read; the full histogram pass runs only when that list misses.
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -172,13 +175,22 @@ __device__ __forceinline__ void load_run(const float4* row4, int n, uint32_t (&k
 // read of the row copies them (order key and index, in ascending index order)
 // into shared memory, and the rest of the selection runs there.  Two reads of
 // the row instead of up to four.
-constexpr int kCap = 3584;
-constexpr int kCapPer = kCap / kThreads;    // 7 list entries a thread orders in the final scan
+constexpr int kCap = 4608;
+constexpr int kCapPer = kCap / kThreads;    // 9 list entries a thread orders in the final scan
+// Rows of at least this many keys start from a sampled lower bound (n / 8 keys
+// sampled, so the sample's target rank stays well inside it for top_k <= 2048).
+constexpr int kSampleMinKeys = 32768;
 static_assert(kCap % kThreads == 0 && kCapPer <= 32, "final scan: one mask bit per entry");
 
-__device__ void collect_and_select(const float4* row4, int n, int n4, uint32_t b1, uint32_t need, int K,
+//
+// With `bound` set, b1 is only a lower bound for the threshold bucket (from a
+// sample of the row): the list then holds every key whose top 12 bits are at
+// least b1, the selection starts from the full key, and the call returns false
+// (nothing written) when the list came out shorter than K (the bound was too
+// high) or longer than kCap.  Returns true once the row's indices are written.
+__device__ bool collect_and_select(const float4* row4, int n, int n4, uint32_t b1, uint32_t need, int K,
                                    int32_t* out, uint32_t* hist, uint32_t* warp_sums, uint32_t* sel,
-                                   uint32_t* c_key, int32_t* c_idx) {
+                                   uint32_t* c_key, int32_t* c_idx, bool bound) {
     const int tid = threadIdx.x;
     // ---- copy keys with top-12 bits >= b1, two coalesced float4 per thread per block step;
     // one scan of (count of float4 0) | (count of float4 1) << 16 orders both.
@@ -219,25 +231,27 @@ __device__ void collect_and_select(const float4* row4, int n, int n4, uint32_t b
         }
         base += (total & 0xFFFFu) + (total >> 16);
     }
+    if (bound && (base < (uint32_t)K || base > (uint32_t)kCap)) return false;   // base is block-uniform
     const int M = min((int)base, kCap);   // = keys above b1 + keys in b1 <= kCap
-    // ---- refine the threshold among the bucket's keys (bits 19..8, then 7..0)
-    uint32_t prefix = b1;
-    int shift = 20;
-    const int digit_bits[2] = {12, 8};
-    for (int pass = 0; pass < 2; ++pass) {
-        const int bits = digit_bits[pass];
+    // ---- refine the threshold among the bucket's keys (bits 19..8, then 7..0); from a bound,
+    // first find the bucket among the list (bits 31..20)
+    uint32_t prefix = bound ? 0u : b1;
+    int shift = bound ? 32 : 20;
+    if (bound) need = (uint32_t)K;
+    for (int pass = bound ? 0 : 1; pass < 3; ++pass) {
+        const int bits = (pass == 2) ? 8 : 12;
         const int nbins = 1 << bits;
         const int new_shift = shift - bits;
         for (int k = tid; k < nbins; k += kThreads) hist[k] = 0u;
         __syncthreads();
         for (int e = tid; e < M; e += kThreads) {
             const uint32_t kk = c_key[e];
-            if ((kk >> shift) == prefix) atomicAdd(&hist[(kk >> new_shift) & (uint32_t)(nbins - 1)], 1u);
+            if (shift == 32 || (kk >> shift) == prefix) atomicAdd(&hist[(kk >> new_shift) & (uint32_t)(nbins - 1)], 1u);
         }
         __syncthreads();
         find_bin(hist, nbins, need, warp_sums, sel);
         const uint32_t bin = sel[0], rem = sel[1], cnt = sel[2];
-        prefix = (prefix << bits) | bin;
+        prefix = (shift == 32 ? 0u : (prefix << bits)) | bin;
         shift = new_shift;
         need = rem;
         __syncthreads();
@@ -274,6 +288,7 @@ __device__ void collect_and_select(const float4* row4, int n, int n4, uint32_t b
         emask &= ~bit;
     }
     __syncthreads();   // the list and the histogram are reused by the next row
+    return true;
 }
 
 // Streaming select (any row length): four CTAs per SM; every pass reads the
@@ -283,8 +298,9 @@ __global__ void __launch_bounds__(kThreads, 4) topk_stream_kernel(const TopkPara
     __shared__ uint32_t hist[kBins];
     __shared__ uint32_t warp_sums[kWarps + 1];
     __shared__ uint32_t sel[3];
-    __shared__ uint32_t c_key[kCollect ? kCap : 1];   // candidate list (ascending key index)
-    __shared__ int32_t c_idx[kCollect ? kCap : 1];
+    extern __shared__ uint32_t dyn_smem[];           // kCollect: the candidate list (ascending key index)
+    uint32_t* c_key = dyn_smem;
+    int32_t* c_idx = reinterpret_cast<int32_t*>(dyn_smem + kCap);
 
     griddep_wait();                 // the scores may still be written by the previous kernel
     const int R = p.B * p.L;
@@ -302,6 +318,33 @@ __global__ void __launch_bounds__(kThreads, 4) topk_stream_kernel(const TopkPara
         const float* row = p.scores + (int64_t)r * p.ld;
         const float4* row4 = reinterpret_cast<const float4*>(row);
         const int n4 = (n + 3) / 4;
+
+        if (kCollect && n >= kSampleMinKeys) {
+            // ---- a lower bound for the threshold bucket from every eighth 128-byte line of the
+            // row (n / 8 keys): the bucket holding the sample's (9 K / 64 + 24)-th largest key,
+            // about 3.5 standard deviations past its expected K / 8 at K = 2048; then one read of
+            // the row copies every key from that bucket up (instead of a full histogram read first)
+            for (int k = threadIdx.x; k < kBins; k += kThreads) hist[k] = 0u;
+            __syncthreads();
+            const int s_f4 = ((n4 + 63) / 64) * 8;   // float4 0..7 of every 64
+            for (int sidx = threadIdx.x; sidx < s_f4; sidx += kThreads) {
+                const int v = 64 * (sidx >> 3) + (sidx & 7);
+                if (v < n4) {
+                    const float4 f = __ldcg(row4 + v);
+                    const float e[4] = {f.x, f.y, f.z, f.w};
+#pragma unroll
+                    for (int k = 0; k < 4; ++k)
+                        if (4 * v + k < n) atomicAdd(&hist[order_key(e[k]) >> 20], 1u);
+                }
+            }
+            __syncthreads();
+            find_bin(hist, kBins, (uint32_t)(p.K + p.K / 8 + 8 * 24) / 8u, warp_sums, sel);
+            const uint32_t b_lo = sel[0];
+            __syncthreads();
+            if (collect_and_select(row4, n, n4, b_lo, 0u, p.K, out, hist, warp_sums, sel, c_key, c_idx, true))
+                continue;
+            __syncthreads();   // fall back to the full passes
+        }
 
         // ---- radix narrowing: (shift, prefix, need) describe the threshold class
         int shift = 32;        // keys compared on bits [shift, 32); 32 = nothing fixed yet
@@ -350,7 +393,7 @@ __global__ void __launch_bounds__(kThreads, 4) topk_stream_kernel(const TopkPara
             }
         }
         if (kCollect && collected) {
-            collect_and_select(row4, n, n4, prefix, need, p.K, out, hist, warp_sums, sel, c_key, c_idx);
+            collect_and_select(row4, n, n4, prefix, need, p.K, out, hist, warp_sums, sel, c_key, c_idx, false);
             continue;
         }
 
@@ -506,10 +549,16 @@ dsa_status_t launch_topk(const float* scores, int64_t ld, const int32_t* q_pos0,
             return DSA_ERR_CUDA;
     } else {
         const int grid = (int)min(R, (long long)device_sm_count() * 4);
-        const cudaError_t e =
-            (Nmax > kChunk)
-                ? launch_pdl(topk_stream_kernel<kLongU, kLongC, true>, dim3(grid), dim3(kThreads), 0, stream, p)
-                : launch_pdl(topk_stream_kernel<1, 1, false>, dim3(grid), dim3(kThreads), 0, stream, p);
+        cudaError_t e;
+        if (Nmax > kChunk) {
+            auto kern = topk_stream_kernel<kLongU, kLongC, true>;
+            constexpr int list_bytes = kCap * 8;   // candidate keys and indices
+            dsa_status_t st = ensure_smem_attr(reinterpret_cast<const void*>(kern), list_bytes);
+            if (st != DSA_OK) return st;
+            e = launch_pdl(kern, dim3(grid), dim3(kThreads), list_bytes, stream, p);
+        } else {
+            e = launch_pdl(topk_stream_kernel<1, 1, false>, dim3(grid), dim3(kThreads), 0, stream, p);
+        }
         if (e != cudaSuccess) return DSA_ERR_CUDA;
     }
     return cudaGetLastError() == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;

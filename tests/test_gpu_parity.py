@@ -148,11 +148,11 @@ def test_topk_long_rows_continuous_scores(dsa, oracle_mod, rows, n):
     np.testing.assert_array_equal(idx.cpu().numpy()[0], ref)
 
 
-@pytest.mark.parametrize("n_tied", [2500, 2584, 2585, 2600])
+@pytest.mark.parametrize("n_tied", [2500, 3608, 3609, 3700])
 def test_topk_long_rows_tie_block_at_list_capacity(dsa, oracle_mod, n_tied):
     """Rows longer than 16384 keys: 1000 keys above a block of n_tied equal keys that holds the
     threshold (1048 of them are taken, lowest indices first), the rest below.  Together they fill
-    the long-row candidate list (3584 entries) up to, exactly at, one past and past its capacity,
+    the long-row candidate list (4608 entries) below, exactly at, one past and past its capacity,
     so both the list path and the streaming fallback decide the ties."""
     n, K, rows = 40000, 2048, 4
     rng = np.random.default_rng(n_tied)
@@ -169,7 +169,26 @@ def test_topk_long_rows_tie_block_at_list_capacity(dsa, oracle_mod, n_tied):
     np.testing.assert_array_equal(idx.cpu().numpy()[0], ref)
 
 
-@pytest.mark.parametrize("n", [4000, 12000, 20000])
+def test_topk_long_rows_sample_misleads_the_bound(dsa, oracle_mod):
+    """Rows of 32768 keys or more start from a lower bound taken from every eighth 128-byte line
+    (keys 256 m .. 256 m + 31).  Here 400 outsized keys sit only in those lines, so the bound lands
+    above all but 400 keys, fewer than top_k: the kernel must notice and select from the full row."""
+    n, K, rows = 40000, 2048, 3
+    rng = np.random.default_rng(99)
+    S = rng.uniform(-1.0, 1.0, (rows, n)).astype(np.float32)
+    sampled = np.nonzero((np.arange(n) // 32) % 8 == 0)[0]
+    for r in range(rows):
+        pick = rng.choice(sampled, size=400, replace=False)
+        S[r, pick] = 100.0 + rng.uniform(0.0, 1.0, 400).astype(np.float32)
+    q_pos0 = np.array([n - rows], np.int32)
+    kv_len = np.array([n], np.int32)
+    idx = dsa.topk(dev(S[None]), dev(q_pos0), dev(kv_len), n, K)
+    torch.cuda.synchronize()
+    ref = oracle_mod.topk(S, q_pos0, kv_len, 1, rows, K)
+    np.testing.assert_array_equal(idx.cpu().numpy()[0], ref)
+
+
+@pytest.mark.parametrize("n", [4000, 12000, 20000, 40000])
 def test_topk_all_equal_and_signed_zero(dsa, oracle_mod, n):
     K, rows = 2048, 3
     S = np.zeros((rows, n), np.float32)
