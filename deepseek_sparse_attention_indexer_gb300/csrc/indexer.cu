@@ -372,6 +372,9 @@ dsa_status_t launch_indexer(const void* q_idx, const void* k_idx, const float* w
     // (the group's queries are loaded once per item).
     const long long groups = (long long)B * p.G;
     long long nc = (4LL * sms + groups - 1) / groups;
+    // A call of at most two tiles per SM (batched decode) is latency bound: one round of items
+    // (about one per SM, their tiles pipelined) beats several rounds of one-tile items.
+    if (groups * p.n_tiles <= 2LL * sms) nc = sms / groups;
     if (nc < 1) nc = 1;
     if (nc > p.n_tiles) nc = p.n_tiles;
     p.CH = ceil_div(p.n_tiles, (int)nc);
