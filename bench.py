@@ -338,6 +338,7 @@ def run_gpu(args, wl, rank, world, local_rank):
     clocks = sampler.stop()
     per = np.array([[evs[k][i].elapsed_time(evs[k][i + 1]) for i in range(3)] for k in range(args.steps)])
     step_ms = float(per.sum(axis=1).mean())
+    step_stats = {"mean": step_ms, "median": float(np.median(per.sum(axis=1))), "min": float(per.sum(axis=1).min())}
     kern_ms = per.mean(axis=0)  # indexer, topk, attention
     step_ms_max = max_over_ranks(step_ms, world, dev)
     status = dsa.device_status()
@@ -477,6 +478,7 @@ def run_gpu(args, wl, rank, world, local_rank):
         "steps": args.steps,
         "warmup": max(3, args.warmup),
         "ms_per_step": step_ms_max,
+        "ms_per_step_stats": step_stats,   # this rank's timed steps: mean (used for value), median, min
         "higher_is_better": hib,
         "scaling": "weak",
         "vs_baseline": None,
