@@ -5,7 +5,8 @@ device copies of the inputs; this module only schedules the host<->device
 copies around them so that they overlap the kernels:
 
   copy stream : indexer inputs | kv | q slice 0 | q slice 1 | ...   (host -> device)
-  compute     :                 indexer | top-k | attn 0 | attn 1 | ...
+  compute     :                 indexer | top-k | attn 0 | attn 2 | ...
+  compute 2   :                                     attn 1 | attn 3 | ...
   copy stream :                                     out 0 |  out 1 | ... (device -> host)
 
 Attention runs per slice of the chunk's queries (each slice is one
@@ -14,8 +15,10 @@ starts as soon as its part of q has landed and its output is copied back while
 the next slice computes.  By default a slice is two rounds of the attention's
 persistent CTAs (2 x the SM count queries): the device->host copy of a slice
 (about 0.11 ms for 304 queries) then keeps pace with the attention, and only
-the last slice's copy trails the compute.  Every step of the method still runs
-in the library's kernels; nothing here computes.
+the last slice's copy trails the compute.  Even and odd slices alternate
+between two streams, so the last round of one slice's persistent CTAs overlaps
+the next slice's start.  Every step of the method still runs in the library's
+kernels; nothing here computes.
 """
 from __future__ import annotations
 
@@ -56,6 +59,7 @@ class HostPrefill:
         self.d_out = torch.empty((L, 64, 512), dtype=torch.bfloat16, device=dev)
         self.copy_in = torch.cuda.Stream(device=dev)
         self.copy_out = torch.cuda.Stream(device=dev)
+        self.attn2 = torch.cuda.Stream(device=dev)   # odd slices: their launch tails overlap the even ones
         per = (L + self.slices - 1) // self.slices
         self.bounds = [(i, min(L, i + per)) for i in range(0, L, per)]
 
@@ -83,15 +87,18 @@ class HostPrefill:
         main.wait_event(ev_idx_in)
         _lib.indexer_scores(self.d_qi, self.d_ki, self.d_w, self.d_pos, self.d_len, scores=self.d_S, stream=main)
         _lib.topk(self.d_S, self.d_pos, self.d_len, self.N, self.top_k, idx=self.d_idx, stream=main)
-        for (a, b), e in zip(self.bounds, ev_q):
-            main.wait_event(e)
+        self.attn2.wait_stream(main)    # the selection is complete for every slice
+        for k, ((a, b), e) in enumerate(zip(self.bounds, ev_q)):
+            st = main if k % 2 == 0 else self.attn2
+            st.wait_event(e)
             _lib.mla_sparse_attn_prefill(self.d_q[0, a:b], self.d_kv[0], self.d_idx[0, a:b], scale,
-                                         out=self.d_out[a:b], stream=main)
+                                         out=self.d_out[a:b], stream=st)
             done = torch.cuda.Event()
-            done.record(main)
+            done.record(st)
             cout.wait_event(done)
             with torch.cuda.stream(cout):
                 h_out[a:b].copy_(self.d_out[a:b], non_blocking=True)
+        main.wait_stream(self.attn2)
         main.wait_stream(cout)      # the chunk ends when its last output slice is on the host
         return h_out
 
