@@ -255,7 +255,13 @@ dsa_status_t mla_sparse_attn_prefill_paged(const void *q, const void *kv_pool,
  *   v     bf16 [R, 64, 256]    output (round to nearest even from float32)
  * bf16 x bf16 products accumulated in float32 by the tensor cores.  R >= 1 rows
  * (a prefill chunk's queries, or one row per sequence in decode).  All three
- * pointers 16-byte aligned.  Needs no workspace.
+ * pointers are caller-owned device memory, 16-byte aligned; o and v must not
+ * overlap.  Needs no workspace.
+ * Errors (host, before any launch): DSA_ERR_INVALID_ARG for a null pointer or
+ * R < 1, DSA_ERR_UNSUPPORTED_SHAPE when R * 64 exceeds 2^31 - 1,
+ * DSA_ERR_MISALIGNED, DSA_ERR_UNSUPPORTED_DEVICE, DSA_ERR_CUDA when the launch
+ * fails.  An in-kernel wait that runs past its limit sets
+ * DSA_ERR_DEVICE_TIMEOUT in the device status word.
  */
 dsa_status_t mla_value_up_proj(const void *o, const void *wv_b, int R, void *v, void *stream);
 
