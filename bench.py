@@ -36,6 +36,18 @@ sys.path.insert(0, ROOT)
 from deepseek_sparse_attention_indexer_gb300 import workloads as W  # noqa: E402
 
 METRIC = "prefill queries/s (indexer+top-k+sparse MLA) at 16k ctx; % of roofline"
+
+
+def metric_name(wl):
+    """The metric string of a workload's line: the headline string for the 16k chunk, the same
+    wording with the workload's own context for the other prefill chunks, a time for decode."""
+    if wl.L == 1:
+        return f"decode us/step (indexer+top-k+sparse MLA, batch {wl.B}, {wl.N} keys)"
+    if wl.name == DEFAULT_WORKLOAD:
+        return METRIC
+    ctx = f"{wl.N // 1024}k" if wl.N % 1024 == 0 else f"{wl.N} keys"
+    return (f"prefill queries/s (indexer+top-k+sparse MLA) at {ctx} ctx "
+            f"({wl.L} queries at positions {wl.p0}..{wl.p0 + wl.L - 1}); % of roofline")
 UNIT = "queries/s"
 DEFAULT_WORKLOAD = "prefill_16k"
 PEAKS_PATH = os.path.join(ROOT, "MEASURED_PEAKS.json")
@@ -122,20 +134,38 @@ def load_peaks():
 
 # ----------------------------------------------------------------------------- clocks
 
+def nvsmi_device_id(local_rank):
+    """The identity nvidia-smi should sample for CUDA device `local_rank`: its UUID (or PCI bus
+    id), which names the same physical GPU whatever CUDA_VISIBLE_DEVICES does to the ordinals.
+    Falls back to the ordinal only when the device reports neither."""
+    import torch
+    props = torch.cuda.get_device_properties(local_rank)
+    uuid = getattr(props, "uuid", None)
+    if uuid:
+        u = str(uuid)
+        return u if u.startswith(("GPU-", "MIG-")) else "GPU-" + u
+    bus = getattr(props, "pci_bus_id", None)
+    if bus is not None:
+        dom = getattr(props, "pci_domain_id", 0) or 0
+        devn = getattr(props, "pci_device_id", 0) or 0
+        return f"{dom:08X}:{bus:02X}:{devn:02X}.0"
+    return str(local_rank)
+
+
 class ClockSampler:
     FIELDS = ("clocks.sm,clocks.max.sm,clocks_event_reasons.hw_slowdown,"
               "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
               "clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, index):
-        self.index = index
+    def __init__(self, device_id):
+        self.device_id = device_id      # UUID or PCI bus id (nvsmi_device_id), not a CUDA ordinal
         self.proc = None
         self.lines = []
 
     def start(self):
         try:
             self.proc = subprocess.Popen(
-                ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.FIELDS,
+                ["nvidia-smi", "-i", str(self.device_id), "--query-gpu=" + self.FIELDS,
                  "--format=csv,noheader,nounits", "-lms", "100"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.thread = threading.Thread(target=self._read, daemon=True)
@@ -149,7 +179,8 @@ class ClockSampler:
 
     def stop(self):
         if self.proc is None:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"],
+                "device": str(self.device_id)}
         self.proc.terminate()
         try:
             self.proc.wait(timeout=5)
@@ -172,7 +203,7 @@ class ClockSampler:
                     reasons.add(n)
         return {"sm_mhz": statistics.median(sm) if sm else None,
                 "sm_max_mhz": max(mx) if mx else None,
-                "reasons": sorted(reasons), "samples": len(sm)}
+                "reasons": sorted(reasons), "samples": len(sm), "device": str(self.device_id)}
 
 
 # ----------------------------------------------------------------------------- oracle (CPU) timing
@@ -216,12 +247,12 @@ def run_reference(args, wl, rank, world):
     tot = 0.0
     for s in range(args.steps):
         tot += oracle_sample(wl, inputs, sample_rows(wl, rows_per_step, 1000 + s), threads)
+    metric = metric_name(wl)
     if decode:
-        metric = f"decode us/step (indexer+top-k+sparse MLA, batch {wl.B}, {wl.N} keys)"
         value, unit, hib = 1e6 * tot / args.steps, "us/step", False
         what = f"all {rows_per_step} sequences of the batch per step, {args.steps} steps"
     else:
-        metric, value, unit, hib = METRIC, rows_per_step * args.steps / tot, UNIT, True
+        value, unit, hib = rows_per_step * args.steps / tot, UNIT, True
         what = (f"{rows_per_step} query rows per step (indexer over all causal keys, top-k, attention over "
                 f"{wl.top_k} keys), {args.steps} steps")
     line = {
@@ -279,7 +310,8 @@ def run_gpu(args, wl, rank, world, local_rank):
     S = torch.empty((wl.B, wl.L, ld), dtype=torch.float32, device=dev)
     idx = torch.empty((wl.B, wl.L, wl.top_k), dtype=torch.int32, device=dev)
     decode = is_decode(wl)
-    out = torch.empty((wl.B if decode else wl.L, 64, 512), dtype=torch.bfloat16, device=dev)
+    # the attention output in float32 (DSA_OUT_F32): the configuration the parity tests check
+    out = torch.empty((wl.B if decode else wl.L, 64, 512), dtype=torch.float32, device=dev)
     ws = torch.empty((dsa.attn_workspace_size(wl.B, wl.top_k),), dtype=torch.uint8, device=dev) if decode else None
     flush = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream()
@@ -319,7 +351,7 @@ def run_gpu(args, wl, rank, world, local_rank):
         raise RuntimeError("device error word set during warm-up")
 
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
-    sampler = ClockSampler(local_rank)
+    sampler = ClockSampler(nvsmi_device_id(local_rank))
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
@@ -380,7 +412,7 @@ def run_gpu(args, wl, rank, world, local_rank):
     # the sequences' key caches (kI, kv) stay resident on the device between steps.
     host_in = [torch.from_numpy(np.ascontiguousarray(a.view(np.int16) if a.dtype == np.uint16 else a)).pin_memory()
                for a in (qi, ki, w, q_pos0, kv_len, q, kv)]
-    host_out = torch.empty(tuple(out.shape), dtype=torch.bfloat16).pin_memory()
+    host_out = torch.empty(tuple(out.shape), dtype=out.dtype).pin_memory()
     dev_in = [h.to(dev) for h in host_in]
     per_step = (0, 2, 3, 4, 5) if decode else range(7)
     h2d = sum(host_in[i].numel() * host_in[i].element_size() for i in per_step)
@@ -389,7 +421,7 @@ def run_gpu(args, wl, rank, world, local_rank):
     if not decode and wl.B == 1:
         # the package's host-buffer prefill: copies on side streams overlap the kernels
         from deepseek_sparse_attention_indexer_gb300.host_prefill import HostPrefill
-        runner = HostPrefill(wl.L, wl.N, wl.top_k, device=dev)
+        runner = HostPrefill(wl.L, wl.N, wl.top_k, device=dev, out_dtype=out.dtype)
         e2e_api = (f"HostPrefill: H2D of the inputs, the three calls and D2H of the output overlapped "
                    f"({runner.slices} query slices)")
 
@@ -423,20 +455,29 @@ def run_gpu(args, wl, rank, world, local_rank):
     e2e_mean = max_over_ranks(float(np.mean(e2e_ms)), world, dev)
 
     # ---- the value up-projection (wv_b) of this step's attention output: the layer's next
-    # call after the path, timed on its own (not part of the metric); L2 flushed before each call
+    # call after the path, timed on its own (not part of the metric); L2 flushed before each call.
+    # It reads bf16 rows: the step's attention output rounded (the library's bf16 output option).
+    out16 = torch.empty(tuple(out.shape), dtype=torch.bfloat16, device=dev)
+    if wl.page_size:
+        dsa.mla_sparse_attn_decode_paged(dq[:, 0], dkv, dlen, dtab, wl.page_size, idx[:, 0], W.SCALE, wl.N,
+                                         out=out16, workspace=ws)
+    elif decode:
+        dsa.mla_sparse_attn_decode(dq[:, 0], dkv, dlen, idx[:, 0], W.SCALE, out=out16, workspace=ws)
+    else:
+        dsa.mla_sparse_attn_prefill(dq[0], dkv[0], idx[0], W.SCALE, out=out16)
     R_v = out.shape[0]
     _, wv_host = W.make_value_proj_inputs(1, seed=wl.seed + 31)
     dwv = d(wv_host)
     vout = torch.empty((R_v, 64, 256), dtype=torch.bfloat16, device=dev)
     for _ in range(3):
-        dsa.mla_value_up_proj(out, dwv, v=vout)
+        dsa.mla_value_up_proj(out16, dwv, v=vout)
     vp_ms = []
     for _ in range(max(3, min(args.steps, 20))):
         flush.zero_()
         e0 = torch.cuda.Event(enable_timing=True)
         e1 = torch.cuda.Event(enable_timing=True)
         e0.record(stream)
-        dsa.mla_value_up_proj(out, dwv, v=vout)
+        dsa.mla_value_up_proj(out16, dwv, v=vout)
         e1.record(stream)
         torch.cuda.synchronize()
         vp_ms.append(e0.elapsed_time(e1))
@@ -455,16 +496,15 @@ def run_gpu(args, wl, rank, world, local_rank):
     attn_name = "mla_sparse_attn_decode" if decode else "mla_sparse_attn_prefill"
     hbm = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
     gather_gbs = work["gather_bytes"] / (kern_ms[2] * 1e-3) / 1e9
+    metric = metric_name(wl)
     if decode:
         # decode: a step is one new token for each of the B sequences; time-like metric
-        metric = f"decode us/step (indexer+top-k+sparse MLA, batch {wl.B}, {wl.N} keys)"
         value, unit, hib = step_ms_max * 1e3, "us/step", False
         e2e_value = e2e_mean * 1e3
         roof = {"bound": "hbm", "kernel": attn_name, "achieved": gather_gbs, "peak": hbm, "unit": "GB/s",
                 "frac": gather_gbs / hbm, "traffic": traffic, "peak_kind": f"{peak_kind} HBM copy",
                 "bytes_per_launch": work["gather_bytes"]}
     else:
-        metric = METRIC
         value, unit, hib = replicas_rate(wl.L * wl.B, world, step_ms_max), UNIT, True
         e2e_value = replicas_rate(wl.L * wl.B, world, e2e_mean)
         roof = {"bound": "tensor", "kernel": attn_name, "achieved": attn_tf, "peak": peak, "unit": "TFLOP/s",
@@ -483,6 +523,7 @@ def run_gpu(args, wl, rank, world, local_rank):
         "scaling": "weak",
         "vs_baseline": None,
         "dtype": "bf16",
+        "attention_output": "float32 (DSA_OUT_F32)",
         "data": "synthetic",
         "config": config_block(wl, world),
         "roofline": roof,

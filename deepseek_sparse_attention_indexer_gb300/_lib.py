@@ -18,6 +18,8 @@ import torch
 from . import _build
 
 DSA_OK = 0
+DSA_OUT_F32 = 0     # attention output element types (include/dsa.h)
+DSA_OUT_BF16 = 1
 STATUS_NAMES = {
     0: "DSA_OK", 1: "DSA_ERR_INVALID_ARG", 2: "DSA_ERR_UNSUPPORTED_SHAPE", 3: "DSA_ERR_MISALIGNED",
     4: "DSA_ERR_WORKSPACE_TOO_SMALL", 5: "DSA_ERR_CUDA", 6: "DSA_ERR_DEVICE_TIMEOUT",
@@ -36,14 +38,15 @@ SIGNATURES = {
     "dsa_indexer_scores": (ctypes.c_int32, [_P, _P, _P, _P, _P, _I, _I, _I, _P, _I64, _P]),
     "dsa_topk_workspace_size": (_SZ, [_I, _I, _I, _I]),
     "dsa_topk": (ctypes.c_int32, [_P, _I64, _P, _P, _I, _I, _I, _I, _P, _P, _SZ, _P]),
-    "mla_sparse_attn_prefill": (ctypes.c_int32, [_P, _P, _P, _I, _I, _I, _F, _P, _P, _P, _SZ, _P]),
+    "mla_sparse_attn_prefill": (ctypes.c_int32, [_P, _P, _P, _I, _I, _I, _F, _P, _I, _P, _P, _SZ, _P]),
     "mla_sparse_attn_workspace_size": (_SZ, [_I, _I, _I, _I]),
-    "mla_sparse_attn_decode": (ctypes.c_int32, [_P, _P, _P, _P, _I, _I, _I, _F, _P, _P, _P, _SZ, _P]),
-    "mla_sparse_attn_decode_noalloc": (ctypes.c_int32, [_P, _P, _P, _P, _I, _I, _I, _F, _P, _P, _P]),
+    "mla_sparse_attn_decode": (ctypes.c_int32, [_P, _P, _P, _P, _I, _I, _I, _F, _P, _I, _P, _P, _SZ, _P]),
+    "mla_sparse_attn_decode_noalloc": (ctypes.c_int32, [_P, _P, _P, _P, _I, _I, _I, _F, _P, _I, _P, _P]),
     "dsa_indexer_scores_paged": (ctypes.c_int32, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _I64, _P]),
-    "mla_sparse_attn_decode_paged": (ctypes.c_int32, [_P, _P, _P, _P, _I, _I, _I, _P, _I, _I, _I, _F, _P, _P, _P,
-                                                      _SZ, _P]),
-    "mla_sparse_attn_prefill_paged": (ctypes.c_int32, [_P, _P, _P, _I, _I, _P, _I, _I, _I, _F, _P, _P, _P, _SZ, _P]),
+    "mla_sparse_attn_decode_paged": (ctypes.c_int32, [_P, _P, _P, _P, _I, _I, _I, _P, _I, _I, _I, _F, _P, _I, _P,
+                                                      _P, _SZ, _P]),
+    "mla_sparse_attn_prefill_paged": (ctypes.c_int32, [_P, _P, _P, _I, _I, _P, _I, _I, _I, _F, _P, _I, _P, _P, _SZ,
+                                                       _P]),
     "mla_value_up_proj": (ctypes.c_int32, [_P, _P, _I, _P, _P]),
     "dsa_indexer_source_layer": (ctypes.c_int, [_I, _I, _I]),
     "dsa_device_status": (ctypes.c_int32, [_P, ctypes.POINTER(ctypes.c_int32), _I]),
@@ -110,6 +113,21 @@ def _is16(t: torch.Tensor) -> bool:
     return t.dtype in (torch.bfloat16, torch.int16, torch.uint16)
 
 
+def _out_dtype(out: torch.Tensor) -> int:
+    """The C ABI's out_dtype for an attention output tensor: float32, or bf16 (or a 16-bit view of it)."""
+    if out.dtype == torch.float32:
+        return DSA_OUT_F32
+    if _is16(out):
+        return DSA_OUT_BF16
+    raise ValueError(f"attention output must be float32 or bf16, got {out.dtype}")
+
+
+def _new_out(rows: int, device, dtype) -> torch.Tensor:
+    if dtype not in (torch.float32, torch.bfloat16):
+        raise ValueError(f"attention output must be float32 or bf16, got {dtype}")
+    return torch.empty((rows, 64, 512), dtype=dtype, device=device)
+
+
 # ----------------------------------------------------------------------------- entry points
 
 def indexer_scores(q_idx: torch.Tensor, k_idx: torch.Tensor, w: torch.Tensor, q_pos0: torch.Tensor,
@@ -142,18 +160,19 @@ def topk(scores: torch.Tensor, q_pos0: torch.Tensor, kv_len: torch.Tensor, Nmax:
 
 def mla_sparse_attn_prefill(q: torch.Tensor, kv: torch.Tensor, idx: torch.Tensor, scale: float,
                             out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
-                            want_lse: bool = False, stream=None):
-    """out [L, 64, 512] bf16 (and lse [L, 64] f32) for q [L,64,576], kv [N,576], idx [L,top_k]."""
+                            want_lse: bool = False, stream=None, out_dtype=torch.float32):
+    """out [L, 64, 512] (float32 by default, or bf16: the float32 result rounded; a given `out`
+    decides) and lse [L, 64] f32, for q [L,64,576], kv [N,576], idx [L,top_k]."""
     L = q.shape[0]
     N = kv.shape[0]
     top_k = idx.shape[-1]
     assert _is16(q) and _is16(kv) and idx.dtype == torch.int32
     if out is None:
-        out = torch.empty((L, 64, 512), dtype=torch.bfloat16, device=q.device)
+        out = _new_out(L, q.device, out_dtype)
     if lse is None and want_lse:
         lse = torch.empty((L, 64), dtype=torch.float32, device=q.device)
     rc = load().mla_sparse_attn_prefill(_ptr(q), _ptr(kv), _ptr(idx), L, N, top_k, float(scale), _ptr(out),
-                                        _ptr(lse), None, 0, _stream(stream))
+                                        _out_dtype(out), _ptr(lse), None, 0, _stream(stream))
     _check("mla_sparse_attn_prefill", rc)
     return (out, lse) if want_lse else out
 
@@ -164,20 +183,22 @@ def attn_workspace_size(B: int, top_k: int, is_decode: bool = True) -> int:
 
 def mla_sparse_attn_decode(q: torch.Tensor, kv: torch.Tensor, kv_len: torch.Tensor, idx: torch.Tensor,
                            scale: float, out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
-                           workspace: Optional[torch.Tensor] = None, want_lse: bool = False, stream=None):
-    """out [B, 64, 512] bf16 for q [B,64,576], kv [B,Nmax,576], kv_len [B], idx [B,top_k]."""
+                           workspace: Optional[torch.Tensor] = None, want_lse: bool = False, stream=None,
+                           out_dtype=torch.float32):
+    """out [B, 64, 512] (float32 by default, or bf16) for q [B,64,576], kv [B,Nmax,576], kv_len [B],
+    idx [B,top_k]."""
     B = q.shape[0]
     Nmax = kv.shape[1]
     top_k = idx.shape[-1]
     if out is None:
-        out = torch.empty((B, 64, 512), dtype=torch.bfloat16, device=q.device)
+        out = _new_out(B, q.device, out_dtype)
     if lse is None and want_lse:
         lse = torch.empty((B, 64), dtype=torch.float32, device=q.device)
     ws_bytes = attn_workspace_size(B, top_k)
     if workspace is None:
         workspace = torch.empty((ws_bytes,), dtype=torch.uint8, device=q.device)
     rc = load().mla_sparse_attn_decode(_ptr(q), _ptr(kv), _ptr(kv_len), _ptr(idx), B, Nmax, top_k, float(scale),
-                                       _ptr(out), _ptr(lse), _ptr(workspace), workspace.numel(),
+                                       _ptr(out), _out_dtype(out), _ptr(lse), _ptr(workspace), workspace.numel(),
                                        _stream(stream))
     _check("mla_sparse_attn_decode", rc)
     return (out, lse) if want_lse else out
@@ -185,7 +206,8 @@ def mla_sparse_attn_decode(q: torch.Tensor, kv: torch.Tensor, kv_len: torch.Tens
 
 def mla_sparse_attn_decode_noalloc(q: torch.Tensor, kv: torch.Tensor, kv_len: torch.Tensor, idx: torch.Tensor,
                                    scale: float, out: Optional[torch.Tensor] = None,
-                                   lse: Optional[torch.Tensor] = None, want_lse: bool = False, stream=None):
+                                   lse: Optional[torch.Tensor] = None, want_lse: bool = False, stream=None,
+                                   out_dtype=torch.float32):
     """Decode attention without a workspace, for callers that may not allocate
     device memory: the library keeps the split partials in its own fixed device
     scratch (B <= 63).  Pass preallocated `out` (and `lse`) to allocate nothing
@@ -194,11 +216,11 @@ def mla_sparse_attn_decode_noalloc(q: torch.Tensor, kv: torch.Tensor, kv_len: to
     Nmax = kv.shape[1]
     top_k = idx.shape[-1]
     if out is None:
-        out = torch.empty((B, 64, 512), dtype=torch.bfloat16, device=q.device)
+        out = _new_out(B, q.device, out_dtype)
     if lse is None and want_lse:
         lse = torch.empty((B, 64), dtype=torch.float32, device=q.device)
     rc = load().mla_sparse_attn_decode_noalloc(_ptr(q), _ptr(kv), _ptr(kv_len), _ptr(idx), B, Nmax, top_k,
-                                               float(scale), _ptr(out), _ptr(lse), _stream(stream))
+                                               float(scale), _ptr(out), _out_dtype(out), _ptr(lse), _stream(stream))
     _check("mla_sparse_attn_decode_noalloc", rc)
     return (out, lse) if want_lse else out
 
@@ -225,7 +247,8 @@ def indexer_scores_paged(q_idx: torch.Tensor, k_pool: torch.Tensor, w: torch.Ten
 def mla_sparse_attn_decode_paged(q: torch.Tensor, kv_pool: torch.Tensor, kv_len: torch.Tensor,
                                  block_table: torch.Tensor, page_size: int, idx: torch.Tensor, scale: float,
                                  Nmax: int, out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
-                                 workspace: Optional[torch.Tensor] = None, want_lse: bool = False, stream=None):
+                                 workspace: Optional[torch.Tensor] = None, want_lse: bool = False, stream=None,
+                                 out_dtype=torch.float32):
     """mla_sparse_attn_decode over a paged cache: kv_pool [num_pages * page_size, 576] bf16,
     block_table [B, bt_stride] int32; idx holds logical key positions."""
     B = q.shape[0]
@@ -233,7 +256,7 @@ def mla_sparse_attn_decode_paged(q: torch.Tensor, kv_pool: torch.Tensor, kv_len:
     assert _is16(q) and _is16(kv_pool) and idx.dtype == torch.int32 and block_table.dtype == torch.int32
     num_pages = kv_pool.shape[0] // page_size
     if out is None:
-        out = torch.empty((B, 64, 512), dtype=torch.bfloat16, device=q.device)
+        out = _new_out(B, q.device, out_dtype)
     if lse is None and want_lse:
         lse = torch.empty((B, 64), dtype=torch.float32, device=q.device)
     ws_bytes = attn_workspace_size(B, top_k)
@@ -241,7 +264,8 @@ def mla_sparse_attn_decode_paged(q: torch.Tensor, kv_pool: torch.Tensor, kv_len:
         workspace = torch.empty((ws_bytes,), dtype=torch.uint8, device=q.device)
     rc = load().mla_sparse_attn_decode_paged(_ptr(q), _ptr(kv_pool), _ptr(kv_len), _ptr(block_table),
                                              block_table.shape[1], page_size, num_pages, _ptr(idx), B, Nmax,
-                                             top_k, float(scale), _ptr(out), _ptr(lse), _ptr(workspace),
+                                             top_k, float(scale), _ptr(out), _out_dtype(out), _ptr(lse),
+                                             _ptr(workspace),
                                              workspace.numel(), _stream(stream))
     _check("mla_sparse_attn_decode_paged", rc)
     return (out, lse) if want_lse else out
@@ -250,7 +274,7 @@ def mla_sparse_attn_decode_paged(q: torch.Tensor, kv_pool: torch.Tensor, kv_len:
 def mla_sparse_attn_prefill_paged(q: torch.Tensor, kv_pool: torch.Tensor, block_table: torch.Tensor,
                                   page_size: int, idx: torch.Tensor, scale: float, N: int,
                                   out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
-                                  want_lse: bool = False, stream=None):
+                                  want_lse: bool = False, stream=None, out_dtype=torch.float32):
     """mla_sparse_attn_prefill over one sequence's paged cache: kv_pool [num_pages * page_size, 576]
     bf16, block_table int32 with ceil(N / page_size) entries; idx holds logical key positions < N."""
     L = q.shape[0]
@@ -258,12 +282,12 @@ def mla_sparse_attn_prefill_paged(q: torch.Tensor, kv_pool: torch.Tensor, block_
     assert _is16(q) and _is16(kv_pool) and idx.dtype == torch.int32 and block_table.dtype == torch.int32
     num_pages = kv_pool.shape[0] // page_size
     if out is None:
-        out = torch.empty((L, 64, 512), dtype=torch.bfloat16, device=q.device)
+        out = _new_out(L, q.device, out_dtype)
     if lse is None and want_lse:
         lse = torch.empty((L, 64), dtype=torch.float32, device=q.device)
     rc = load().mla_sparse_attn_prefill_paged(_ptr(q), _ptr(kv_pool), _ptr(block_table), page_size, num_pages,
-                                              _ptr(idx), L, N, top_k, float(scale), _ptr(out), _ptr(lse), None, 0,
-                                              _stream(stream))
+                                              _ptr(idx), L, N, top_k, float(scale), _ptr(out), _out_dtype(out),
+                                              _ptr(lse), None, 0, _stream(stream))
     _check("mla_sparse_attn_prefill_paged", rc)
     return (out, lse) if want_lse else out
 

@@ -216,11 +216,12 @@ size_t mla_sparse_attn_workspace_size(int B, int L, int top_k, int is_decode) {
 }
 
 dsa_status_t mla_sparse_attn_prefill(const void* q, const void* kv, const int32_t* idx, int L, int N, int top_k,
-                                     float scale, void* out, float* lse, void* workspace, size_t ws_bytes,
-                                     void* stream) {
+                                     float scale, void* out, int out_dtype, float* lse, void* workspace,
+                                     size_t ws_bytes, void* stream) {
     (void)workspace;
     (void)ws_bytes;
     if (!q || !kv || !idx || !out) return DSA_ERR_INVALID_ARG;
+    if (out_dtype != DSA_OUT_F32 && out_dtype != DSA_OUT_BF16) return DSA_ERR_INVALID_ARG;
     if (L < 1 || N < 1) return DSA_ERR_INVALID_ARG;
     if (top_k < 1 || top_k > DSA_MAX_TOPK) return DSA_ERR_UNSUPPORTED_SHAPE;
     if ((long long)L * DSA_HEADS > 0x7FFFFFFFLL) return DSA_ERR_UNSUPPORTED_SHAPE;
@@ -228,16 +229,18 @@ dsa_status_t mla_sparse_attn_prefill(const void* q, const void* kv, const int32_
     if (!aligned16(q) || !aligned16(kv) || !aligned16(out)) return DSA_ERR_MISALIGNED;
     dsa_status_t st = check_device();
     if (st != DSA_OK) return st;
-    return launch_attn_prefill(q, kv, idx, L, N, top_k, scale, out, lse, PageTable{}, static_cast<cudaStream_t>(stream));
+    return launch_attn_prefill(q, kv, idx, L, N, top_k, scale, out, out_dtype == DSA_OUT_F32, lse, PageTable{},
+                               static_cast<cudaStream_t>(stream));
 }
 
 dsa_status_t mla_sparse_attn_prefill_paged(const void* q, const void* kv_pool, const int32_t* block_table,
                                            int page_size, int num_pages, const int32_t* idx, int L, int N,
-                                           int top_k, float scale, void* out, float* lse, void* workspace,
-                                           size_t ws_bytes, void* stream) {
+                                           int top_k, float scale, void* out, int out_dtype, float* lse,
+                                           void* workspace, size_t ws_bytes, void* stream) {
     (void)workspace;
     (void)ws_bytes;
     if (!q || !kv_pool || !idx || !out) return DSA_ERR_INVALID_ARG;
+    if (out_dtype != DSA_OUT_F32 && out_dtype != DSA_OUT_BF16) return DSA_ERR_INVALID_ARG;
     if (L < 1 || N < 1) return DSA_ERR_INVALID_ARG;
     if (top_k < 1 || top_k > DSA_MAX_TOPK) return DSA_ERR_UNSUPPORTED_SHAPE;
     if ((long long)L * DSA_HEADS > 0x7FFFFFFFLL) return DSA_ERR_UNSUPPORTED_SHAPE;
@@ -249,13 +252,15 @@ dsa_status_t mla_sparse_attn_prefill_paged(const void* q, const void* kv_pool, c
     if (st != DSA_OK) return st;
     if (!aligned16(q) || !aligned16(kv_pool) || !aligned16(out)) return DSA_ERR_MISALIGNED;
     if ((st = check_device()) != DSA_OK) return st;
-    return launch_attn_prefill(q, kv_pool, idx, L, N, top_k, scale, out, lse, pt, static_cast<cudaStream_t>(stream));
+    return launch_attn_prefill(q, kv_pool, idx, L, N, top_k, scale, out, out_dtype == DSA_OUT_F32, lse, pt,
+                               static_cast<cudaStream_t>(stream));
 }
 
 dsa_status_t mla_sparse_attn_decode(const void* q, const void* kv, const int32_t* kv_len, const int32_t* idx, int B,
-                                    int Nmax, int top_k, float scale, void* out, float* lse, void* workspace,
-                                    size_t ws_bytes, void* stream) {
+                                    int Nmax, int top_k, float scale, void* out, int out_dtype, float* lse,
+                                    void* workspace, size_t ws_bytes, void* stream) {
     if (!q || !kv || !kv_len || !idx || !out || !workspace) return DSA_ERR_INVALID_ARG;
+    if (out_dtype != DSA_OUT_F32 && out_dtype != DSA_OUT_BF16) return DSA_ERR_INVALID_ARG;
     if (B < 1 || Nmax < 1) return DSA_ERR_INVALID_ARG;
     if (top_k < 1 || top_k > DSA_MAX_TOPK) return DSA_ERR_UNSUPPORTED_SHAPE;
     if (!(scale > 0.f) || !(scale < 1e30f)) return DSA_ERR_INVALID_ARG;
@@ -263,15 +268,17 @@ dsa_status_t mla_sparse_attn_decode(const void* q, const void* kv, const int32_t
     if (ws_bytes < attn_decode_workspace(B, top_k)) return DSA_ERR_WORKSPACE_TOO_SMALL;
     dsa_status_t st = check_device();
     if (st != DSA_OK) return st;
-    return launch_attn_decode(q, kv, kv_len, idx, B, Nmax, top_k, scale, out, lse, workspace, PageTable{},
-                              static_cast<cudaStream_t>(stream));
+    return launch_attn_decode(q, kv, kv_len, idx, B, Nmax, top_k, scale, out, out_dtype == DSA_OUT_F32, lse,
+                              workspace, PageTable{}, static_cast<cudaStream_t>(stream));
 }
 
 dsa_status_t mla_sparse_attn_decode_paged(const void* q, const void* kv_pool, const int32_t* kv_len,
                                           const int32_t* block_table, int bt_stride, int page_size, int num_pages,
                                           const int32_t* idx, int B, int Nmax, int top_k, float scale, void* out,
-                                          float* lse, void* workspace, size_t ws_bytes, void* stream) {
+                                          int out_dtype, float* lse, void* workspace, size_t ws_bytes,
+                                          void* stream) {
     if (!q || !kv_pool || !kv_len || !idx || !out || !workspace) return DSA_ERR_INVALID_ARG;
+    if (out_dtype != DSA_OUT_F32 && out_dtype != DSA_OUT_BF16) return DSA_ERR_INVALID_ARG;
     if (B < 1 || Nmax < 1) return DSA_ERR_INVALID_ARG;
     if (top_k < 1 || top_k > DSA_MAX_TOPK) return DSA_ERR_UNSUPPORTED_SHAPE;
     if (!(scale > 0.f) || !(scale < 1e30f)) return DSA_ERR_INVALID_ARG;
@@ -282,14 +289,15 @@ dsa_status_t mla_sparse_attn_decode_paged(const void* q, const void* kv_pool, co
     if (!aligned16(q) || !aligned16(kv_pool) || !aligned16(out) || !aligned16(workspace)) return DSA_ERR_MISALIGNED;
     if (ws_bytes < attn_decode_workspace(B, top_k)) return DSA_ERR_WORKSPACE_TOO_SMALL;
     if ((st = check_device()) != DSA_OK) return st;
-    return launch_attn_decode(q, kv_pool, kv_len, idx, B, Nmax, top_k, scale, out, lse, workspace, pt,
-                              static_cast<cudaStream_t>(stream));
+    return launch_attn_decode(q, kv_pool, kv_len, idx, B, Nmax, top_k, scale, out, out_dtype == DSA_OUT_F32, lse,
+                              workspace, pt, static_cast<cudaStream_t>(stream));
 }
 
 dsa_status_t mla_sparse_attn_decode_noalloc(const void* q, const void* kv, const int32_t* kv_len,
                                             const int32_t* idx, int B, int Nmax, int top_k, float scale, void* out,
-                                            float* lse, void* stream) {
+                                            int out_dtype, float* lse, void* stream) {
     if (!q || !kv || !kv_len || !idx || !out) return DSA_ERR_INVALID_ARG;
+    if (out_dtype != DSA_OUT_F32 && out_dtype != DSA_OUT_BF16) return DSA_ERR_INVALID_ARG;
     if (B < 1 || Nmax < 1) return DSA_ERR_INVALID_ARG;
     if (top_k < 1 || top_k > DSA_MAX_TOPK) return DSA_ERR_UNSUPPORTED_SHAPE;
     if (!(scale > 0.f) || !(scale < 1e30f)) return DSA_ERR_INVALID_ARG;
@@ -297,8 +305,8 @@ dsa_status_t mla_sparse_attn_decode_noalloc(const void* q, const void* kv, const
     if (B > DSA_NOALLOC_MAX_BATCH) return DSA_ERR_SCRATCH_TOO_SMALL;
     dsa_status_t st = check_device();
     if (st != DSA_OK) return st;
-    return launch_attn_decode_noalloc(q, kv, kv_len, idx, B, Nmax, top_k, scale, out, lse,
-                                      static_cast<cudaStream_t>(stream));
+    return launch_attn_decode_noalloc(q, kv, kv_len, idx, B, Nmax, top_k, scale, out, out_dtype == DSA_OUT_F32,
+                                      lse, static_cast<cudaStream_t>(stream));
 }
 
 dsa_status_t mla_value_up_proj(const void* o, const void* wv_b, int R, void* v, void* stream) {

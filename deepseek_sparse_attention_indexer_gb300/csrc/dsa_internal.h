@@ -68,14 +68,15 @@ dsa_status_t launch_indexer(const void* q_idx, const void* k_idx, const float* w
 dsa_status_t launch_topk(const float* scores, int64_t ld, const int32_t* q_pos0, const int32_t* kv_len, int B,
                          int L, int Nmax, int top_k, int32_t* idx, cudaStream_t stream);
 dsa_status_t launch_attn_prefill(const void* q, const void* kv, const int32_t* idx, int L, int N, int top_k,
-                                 float scale, void* out, float* lse, const PageTable& pages, cudaStream_t stream);
+                                 float scale, void* out, int out_f32, float* lse, const PageTable& pages,
+                                 cudaStream_t stream);
 size_t attn_decode_workspace(int B, int top_k);
 dsa_status_t launch_attn_decode_noalloc(const void* q, const void* kv, const int32_t* kv_len, const int32_t* idx,
-                                        int B, int Nmax, int top_k, float scale, void* out, float* lse,
-                                        cudaStream_t stream);
+                                        int B, int Nmax, int top_k, float scale, void* out, int out_f32,
+                                        float* lse, cudaStream_t stream);
 dsa_status_t launch_attn_decode(const void* q, const void* kv, const int32_t* kv_len, const int32_t* idx, int B,
-                                int Nmax, int top_k, float scale, void* out, float* lse, void* workspace,
-                                const PageTable& pages, cudaStream_t stream);
+                                int Nmax, int top_k, float scale, void* out, int out_f32, float* lse,
+                                void* workspace, const PageTable& pages, cudaStream_t stream);
 dsa_status_t launch_value_up_proj(const void* o, const void* wv_b, int R, void* v, cudaStream_t stream);
 
 }  // namespace dsa

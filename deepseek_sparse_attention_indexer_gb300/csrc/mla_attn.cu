@@ -105,7 +105,8 @@ struct AttnParams {
     const __nv_bfloat16* kv;   // [B][Nmax][576]
     const int32_t* idx;        // [rows][top_k]
     const int32_t* kv_len;     // [B] or nullptr (then every row may use Nmax keys)
-    __nv_bfloat16* out;        // final: [rows][64][512]
+    void* out;                 // final: [rows][64][512], float32 or bf16 (out_f32)
+    int out_f32;               // 1: float32 output; 0: bf16 (round to nearest even)
     float* lse;                // final: [rows][64] or nullptr
     float* part_o;             // partial: [rows][nsplit][64][512]
     float* part_lse;           // partial: [rows][nsplit][64]
@@ -475,31 +476,33 @@ __global__ void __launch_bounds__(kThreads, 1)   // 18 warps: at most 96 registe
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(s_empty);
-                if (!((j >= 0) && (j < I.bound))) {
+                const bool kvalid = (j >= 0) && (j < I.bound);
+                // Reference maxima (scaled, log2 units), one per head: set from the item's
+                // first tile, afterwards moved only when a score exceeds its head's reference
+                // by more than 2^16 (checked per thread; rare), so the common path has no
+                // cross-thread reduction.  The shifted exponent e = scale*log2(e)*s - m serves
+                // both the check and the probability.  Before the first tile every reference
+                // is -inf, so any valid score counts as exceeding it.  The scale is > 0, so
+                // maxima of the raw scores are maxima of the scaled ones.
+                float mr[kHG];
 #pragma unroll
-                    for (int h = 0; h < kHG; ++h) x[h] = -INFINITY;
+                for (int h4 = 0; h4 < kHG / 4; ++h4) {
+                    const float4 m4 = reinterpret_cast<const float4*>(m_used + h0)[h4];
+                    mr[4 * h4 + 0] = m4.x;
+                    mr[4 * h4 + 1] = m4.y;
+                    mr[4 * h4 + 2] = m4.z;
+                    mr[4 * h4 + 3] = m4.w;
                 }
-                // Reference maxima (scaled, log2 units): set from the item's first tile.
-                // Afterwards a head's reference only moves when one of its scores exceeds
-                // it by more than 2^16 (checked per thread; rare), so the common path has
-                // no cross-thread reduction.  The scale is > 0, so maxima of the raw
-                // scores are maxima of the scaled ones.
-                bool need_red = (t == 0);
-                if (!need_red) {
-                    bool viol = false;
+                bool viol = false;
 #pragma unroll
-                    for (int h4 = 0; h4 < kHG / 4; ++h4) {
-                        const float4 m4 = reinterpret_cast<const float4*>(m_used + h0)[h4];
-                        viol |= x[4 * h4 + 0] * p.scale_log2 > m4.x + kRescaleThreshold;
-                        viol |= x[4 * h4 + 1] * p.scale_log2 > m4.y + kRescaleThreshold;
-                        viol |= x[4 * h4 + 2] * p.scale_log2 > m4.z + kRescaleThreshold;
-                        viol |= x[4 * h4 + 3] * p.scale_log2 > m4.w + kRescaleThreshold;
-                    }
-                    need_red = named_bar_or(group_bar, kGroupThreads, viol);
-                }
+                for (int h = 0; h < kHG; ++h) viol |= kvalid && (fmaf(x[h], p.scale_log2, -mr[h]) > kRescaleThreshold);
+                const bool need_red = named_bar_or(group_bar, kGroupThreads, viol);
                 bool any_upd = false;
                 if (need_red) {
-                    const float r = warp_transpose_reduce16<true>(x, lane);
+                    float xm[kHG];
+#pragma unroll
+                    for (int h = 0; h < kHG; ++h) xm[h] = kvalid ? x[h] : -INFINITY;
+                    const float r = warp_transpose_reduce16<true>(xm, lane);
                     if ((lane & 1u) == 0) red[quad * kH + h0 + (int)(lane >> 1)] = r;
                     named_bar_sync(group_bar, kGroupThreads);
                     bool upd = false;
@@ -516,28 +519,35 @@ __global__ void __launch_bounds__(kThreads, 1)   // 18 warps: at most 96 registe
                         alpha_s[h] = a;
                     }
                     any_upd = named_bar_or(group_bar, kGroupThreads, upd);
+#pragma unroll
+                    for (int h4 = 0; h4 < kHG / 4; ++h4) {
+                        const float4 m4 = reinterpret_cast<const float4*>(m_used + h0)[h4];
+                        mr[4 * h4 + 0] = m4.x;
+                        mr[4 * h4 + 1] = m4.y;
+                        mr[4 * h4 + 2] = m4.z;
+                        mr[4 * h4 + 3] = m4.w;
+                    }
+                    if (any_upd) {
+#pragma unroll
+                        for (int h4 = 0; h4 < kHG / 4; ++h4) {
+                            const float4 a4 = reinterpret_cast<const float4*>(alpha_s + h0)[h4];
+                            l_part[4 * h4 + 0] *= a4.x;
+                            l_part[4 * h4 + 1] *= a4.y;
+                            l_part[4 * h4 + 2] *= a4.z;
+                            l_part[4 * h4 + 3] *= a4.w;
+                        }
+                    }
                 }
-                // probabilities (bf16 for the MMA, float32 for the row sum)
+                // Probabilities: float32 into the row sum (so lse is the log of the exact sum),
+                // rounded to bf16 for the MMA.
                 uint32_t packed[kHG / 2];
 #pragma unroll
-                for (int h4 = 0; h4 < kHG / 4; ++h4) {
-                    const float4 m4 = reinterpret_cast<const float4*>(m_used + h0)[h4];
-                    const float mm[4] = {m4.x, m4.y, m4.z, m4.w};
-                    float pr[4];
-#pragma unroll
-                    for (int k = 0; k < 4; ++k)
-                        pr[k] = ex2_approx(fmaf(x[4 * h4 + k], p.scale_log2, (mm[k] == -INFINITY) ? 0.f : -mm[k]));
-                    if (any_upd) {
-                        const float4 a4 = reinterpret_cast<const float4*>(alpha_s + h0)[h4];
-                        l_part[4 * h4 + 0] *= a4.x;
-                        l_part[4 * h4 + 1] *= a4.y;
-                        l_part[4 * h4 + 2] *= a4.z;
-                        l_part[4 * h4 + 3] *= a4.w;
-                    }
-#pragma unroll
-                    for (int k = 0; k < 4; ++k) l_part[4 * h4 + k] += pr[k];
-                    packed[2 * h4] = pack_bf16x2(pr[0], pr[1]);
-                    packed[2 * h4 + 1] = pack_bf16x2(pr[2], pr[3]);
+                for (int h2 = 0; h2 < kHG / 2; ++h2) {
+                    const float p0 = ex2_approx(kvalid ? fmaf(x[2 * h2], p.scale_log2, -mr[2 * h2]) : -INFINITY);
+                    const float p1 = ex2_approx(kvalid ? fmaf(x[2 * h2 + 1], p.scale_log2, -mr[2 * h2 + 1]) : -INFINITY);
+                    packed[h2] = pack_bf16x2(p0, p1);
+                    l_part[2 * h2] += p0;
+                    l_part[2 * h2 + 1] += p1;
                 }
                 // P^T row `key`, heads h0..h0+15: 16-byte chunks 2hg and 2hg+1 of the swizzled 128-byte row
 #pragma unroll
@@ -605,8 +615,12 @@ __global__ void __launch_bounds__(kThreads, 1)   // 18 warps: at most 96 registe
                     float* dst = p.part_o + (((int64_t)I.row * p.nsplit + I.split) * kH + h0) * kDv + dim;
 #pragma unroll
                     for (int h = 0; h < kHG; ++h) dst[h * kDv] = o[h];
+                } else if (p.out_f32) {
+                    float* dst = static_cast<float*>(p.out) + ((int64_t)I.row * kH + h0) * kDv + dim;
+#pragma unroll
+                    for (int h = 0; h < kHG; ++h) dst[h * kDv] = o[h];
                 } else {
-                    __nv_bfloat16* dst = p.out + ((int64_t)I.row * kH + h0) * kDv + dim;
+                    __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(p.out) + ((int64_t)I.row * kH + h0) * kDv + dim;
 #pragma unroll
                     for (int h = 0; h < kHG; ++h) dst[h * kDv] = __float2bfloat16_rn(o[h]);
                 }
@@ -635,7 +649,7 @@ __global__ void __launch_bounds__(kThreads, 1)   // 18 warps: at most 96 registe
 // slots per split); every thread issues all of its split loads before using any.
 constexpr int kMaxSplits = DSA_MAX_TOPK / kTile;
 __global__ void __launch_bounds__(128) mla_decode_combine_kernel(const float* part_o, const float* part_lse,
-                                                                 int nsplit, __nv_bfloat16* out, float* lse) {
+                                                                 int nsplit, void* out, int out_f32, float* lse) {
     griddep_wait();
     const int b = blockIdx.x / kH, h = blockIdx.x % kH;
     const float* pl = part_lse + (int64_t)b * nsplit * kH + h;
@@ -662,11 +676,17 @@ __global__ void __launch_bounds__(128) mla_decode_combine_kernel(const float* pa
         acc.w += wgt * v[s].w;
     }
     const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
-    __nv_bfloat16* dst = out + ((int64_t)b * kH + h) * kDv + 4 * threadIdx.x;
-    dst[0] = __float2bfloat16_rn(acc.x * inv);
-    dst[1] = __float2bfloat16_rn(acc.y * inv);
-    dst[2] = __float2bfloat16_rn(acc.z * inv);
-    dst[3] = __float2bfloat16_rn(acc.w * inv);
+    const int64_t o = ((int64_t)b * kH + h) * kDv + 4 * threadIdx.x;
+    if (out_f32) {
+        reinterpret_cast<float4*>(static_cast<float*>(out) + o)[0] =
+            make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+    } else {
+        __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(out) + o;
+        dst[0] = __float2bfloat16_rn(acc.x * inv);
+        dst[1] = __float2bfloat16_rn(acc.y * inv);
+        dst[2] = __float2bfloat16_rn(acc.z * inv);
+        dst[3] = __float2bfloat16_rn(acc.w * inv);
+    }
     if (lse && threadIdx.x == 0) lse[(int64_t)b * kH + h] = wsum > 0.f ? M + logf(wsum) : -INFINITY;
 }
 
@@ -693,12 +713,14 @@ int decode_splits(int B, int top_k) {
 }  // namespace
 
 dsa_status_t launch_attn_prefill(const void* q, const void* kv, const int32_t* idx, int L, int N, int top_k,
-                                 float scale, void* out, float* lse, const PageTable& pages, cudaStream_t stream) {
+                                 float scale, void* out, int out_f32, float* lse, const PageTable& pages,
+                                 cudaStream_t stream) {
     AttnParams p{};
     p.kv = static_cast<const __nv_bfloat16*>(kv);
     p.idx = idx;
     p.kv_len = nullptr;
-    p.out = static_cast<__nv_bfloat16*>(out);
+    p.out = out;
+    p.out_f32 = out_f32;
     p.lse = lse;
     p.rows = L;
     p.prefill = 1;
@@ -719,8 +741,8 @@ size_t attn_decode_workspace(int B, int top_k) {
 }
 
 dsa_status_t launch_attn_decode(const void* q, const void* kv, const int32_t* kv_len, const int32_t* idx, int B,
-                                int Nmax, int top_k, float scale, void* out, float* lse, void* workspace,
-                                const PageTable& pages, cudaStream_t stream) {
+                                int Nmax, int top_k, float scale, void* out, int out_f32, float* lse,
+                                void* workspace, const PageTable& pages, cudaStream_t stream) {
     const int ns = decode_splits(B, top_k);
     const int tiles = ceil_div(top_k, kTile);
     AttnParams p{};
@@ -743,7 +765,7 @@ dsa_status_t launch_attn_decode(const void* q, const void* kv, const int32_t* kv
     dsa_status_t st = p.pages.table ? launch_kernel<true, true>(q, B, p, stream) : launch_kernel<true, false>(q, B, p, stream);
     if (st != DSA_OK) return st;
     if (launch_pdl(mla_decode_combine_kernel, dim3(B * kH), dim3(128), 0, stream, (const float*)p.part_o,
-                   (const float*)p.part_lse, p.nsplit, static_cast<__nv_bfloat16*>(out), lse) != cudaSuccess)
+                   (const float*)p.part_lse, p.nsplit, out, out_f32, lse) != cudaSuccess)
         return DSA_ERR_CUDA;
     return cudaGetLastError() == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
 }
@@ -779,8 +801,8 @@ dsa_status_t noalloc_scratch(void** ptr) {
 }  // namespace
 
 dsa_status_t launch_attn_decode_noalloc(const void* q, const void* kv, const int32_t* kv_len, const int32_t* idx,
-                                        int B, int Nmax, int top_k, float scale, void* out, float* lse,
-                                        cudaStream_t stream) {
+                                        int B, int Nmax, int top_k, float scale, void* out, int out_f32,
+                                        float* lse, cudaStream_t stream) {
     const size_t per_item = (size_t)kH * (kDv + 1) * sizeof(float);
     const int max_items = (int)(kNoallocScratchBytes / per_item);
     if (B > max_items) return DSA_ERR_SCRATCH_TOO_SMALL;
@@ -809,7 +831,7 @@ dsa_status_t launch_attn_decode_noalloc(const void* q, const void* kv, const int
     st = launch_kernel<true, false>(q, B, p, stream);
     if (st != DSA_OK) return st;
     if (launch_pdl(mla_decode_combine_kernel, dim3(B * kH), dim3(128), 0, stream, (const float*)p.part_o,
-                   (const float*)p.part_lse, p.nsplit, static_cast<__nv_bfloat16*>(out), lse) != cudaSuccess)
+                   (const float*)p.part_lse, p.nsplit, out, out_f32, lse) != cudaSuccess)
         return DSA_ERR_CUDA;
     return cudaGetLastError() == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
 }

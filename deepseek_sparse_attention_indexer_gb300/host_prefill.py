@@ -38,7 +38,8 @@ class HostPrefill:
     for the copies to be asynchronous.
     """
 
-    def __init__(self, L: int, N: int, top_k: int, device=None, slices: Optional[int] = None):
+    def __init__(self, L: int, N: int, top_k: int, device=None, slices: Optional[int] = None,
+                 out_dtype=torch.float32):
         self.L, self.N, self.top_k = L, N, top_k
         self.dev = torch.device(device if device is not None else "cuda")
         if slices is None:   # two rounds of one attention CTA per SM a slice
@@ -56,7 +57,7 @@ class HostPrefill:
         ld = (N + 3) // 4 * 4
         self.d_S = torch.empty((1, L, ld), dtype=torch.float32, device=dev)
         self.d_idx = torch.empty((1, L, top_k), dtype=torch.int32, device=dev)
-        self.d_out = torch.empty((L, 64, 512), dtype=torch.bfloat16, device=dev)
+        self.d_out = torch.empty((L, 64, 512), dtype=out_dtype, device=dev)
         self.copy_in = torch.cuda.Stream(device=dev)
         self.copy_out = torch.cuda.Stream(device=dev)
         self.attn2 = torch.cuda.Stream(device=dev)   # odd slices: their launch tails overlap the even ones
@@ -97,7 +98,7 @@ class HostPrefill:
             done.record(st)
             cout.wait_event(done)
             with torch.cuda.stream(cout):
-                h_out[a:b].copy_(self.d_out[a:b], non_blocking=True)
+                _as(h_out, self.d_out)[a:b].copy_(self.d_out[a:b], non_blocking=True)
         main.wait_stream(self.attn2)
         main.wait_stream(cout)      # the chunk ends when its last output slice is on the host
         return h_out

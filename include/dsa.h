@@ -34,7 +34,8 @@
 extern "C" {
 #endif
 
-#define DSA_ABI_VERSION 3  /* 2: paged-cache entry points; 3: value up-projection, indexer layer schedule */
+#define DSA_ABI_VERSION 4  /* 2: paged-cache entry points; 3: value up-projection, indexer layer schedule;
+                              4: attention output element type (out_dtype) */
 
 #define DSA_INDEXER_HEADS 32
 #define DSA_INDEXER_DIM 128
@@ -58,6 +59,20 @@ enum {
     DSA_ERR_UNSUPPORTED_DEVICE = 8,  /* current device is not compute capability 10.3 */
     DSA_ERR_SCRATCH_TOO_SMALL = 9    /* request does not fit the library's fixed device scratch */
 };
+
+/*
+ * Element type of an attention output buffer (the out_dtype argument of the
+ * mla_sparse_attn_* calls).  The pages fix the softmax in float32 (exo PR
+ * #2539, section "Prefill") but not the type of the attention output; in the
+ * llama.cpp graph on the SlimServe page ("GLM52_PIPELINE_TRACE.md", section 6)
+ * the output kqv = mul_mat(v, kq) is a float32 product that feeds the wv_b
+ * up-projection.  DSA_OUT_F32 returns that float32 result.  DSA_OUT_BF16
+ * returns the same float32 result rounded to nearest even, for a bf16
+ * consumer (such as mla_value_up_proj); the rounding alone moves each element
+ * by up to 2^-9 of its magnitude.
+ */
+#define DSA_OUT_F32 0
+#define DSA_OUT_BF16 1
 
 /* Text for a status code (static storage, never NULL). */
 const char *dsa_status_string(dsa_status_t status);
@@ -123,15 +138,22 @@ dsa_status_t dsa_topk(const float *scores, int64_t ld, const int32_t *q_pos0,
  *   kv   bf16 [N, 576]         latent cache rows [kv_cmpr | k_pe]
  *   idx  int32 [L, top_k]      selected keys (from dsa_topk); entries >= N are
  *                              recorded as DSA_ERR_DEVICE_BOUNDS and skipped
- *   out  bf16 [L, 64, 512]     output (round to nearest even from float32)
+ *   out  [L, 64, 512]          output: float32 (out_dtype DSA_OUT_F32) or bf16
+ *                              (DSA_OUT_BF16, the float32 result rounded to nearest even)
  *   lse  f32 [L, 64] or NULL   natural-log sum of exp of the scaled scores
+ * The scores, the softmax and both sums are float32; the probabilities enter the
+ * value product as bf16 (the tensor-core operand type of the latent rows).
  * A row with no selected key writes zeros and lse = -inf.
  * scale is the softmax scale (1/sqrt(192 + 64) = 1/16 for GLM-5.x).
  * Needs no workspace for prefill (pass NULL, 0).
+ * Errors: DSA_ERR_INVALID_ARG for a null pointer, L < 1, N < 1, a scale that
+ * is not a positive finite number or an out_dtype other than DSA_OUT_F32 /
+ * DSA_OUT_BF16; DSA_ERR_UNSUPPORTED_SHAPE for top_k outside 1..2048;
+ * DSA_ERR_MISALIGNED for q, kv or out not 16-byte aligned.
  */
 dsa_status_t mla_sparse_attn_prefill(const void *q, const void *kv, const int32_t *idx, int L,
-                                     int N, int top_k, float scale, void *out, float *lse,
-                                     void *workspace, size_t ws_bytes, void *stream);
+                                     int N, int top_k, float scale, void *out, int out_dtype,
+                                     float *lse, void *workspace, size_t ws_bytes, void *stream);
 
 /*
  * mla_sparse_attn_decode -- the same attention for one new token in each of B
@@ -143,15 +165,15 @@ dsa_status_t mla_sparse_attn_prefill(const void *q, const void *kv, const int32_
  *
  *   q       bf16 [B, 64, 576]; kv bf16 [B, Nmax, 576]; kv_len int32 [B] (device)
  *   idx     int32 [B, top_k]   (entries >= kv_len[b] recorded as bounds errors, skipped)
- *   out     bf16 [B, 64, 512]; lse f32 [B, 64] or NULL
+ *   out     [B, 64, 512] float32 or bf16 (out_dtype, as for prefill); lse f32 [B, 64] or NULL
  *   workspace  device buffer of at least mla_sparse_attn_workspace_size(B, 1, top_k, 1)
  *              bytes, 16-byte aligned; its contents need no initialisation.
  */
 size_t mla_sparse_attn_workspace_size(int B, int L, int top_k, int is_decode);
 dsa_status_t mla_sparse_attn_decode(const void *q, const void *kv, const int32_t *kv_len,
                                     const int32_t *idx, int B, int Nmax, int top_k, float scale,
-                                    void *out, float *lse, void *workspace, size_t ws_bytes,
-                                    void *stream);
+                                    void *out, int out_dtype, float *lse, void *workspace,
+                                    size_t ws_bytes, void *stream);
 
 /*
  * mla_sparse_attn_decode_noalloc -- mla_sparse_attn_decode for callers that
@@ -186,7 +208,8 @@ dsa_status_t mla_sparse_attn_decode(const void *q, const void *kv, const int32_t
 #define DSA_NOALLOC_MAX_BATCH 63
 dsa_status_t mla_sparse_attn_decode_noalloc(const void *q, const void *kv, const int32_t *kv_len,
                                             const int32_t *idx, int B, int Nmax, int top_k,
-                                            float scale, void *out, float *lse, void *stream);
+                                            float scale, void *out, int out_dtype, float *lse,
+                                            void *stream);
 
 /*
  * Paged caches.  Serving engines keep each sequence's cache rows in fixed-size
@@ -225,8 +248,9 @@ dsa_status_t dsa_indexer_scores_paged(const void *q_idx, const void *k_pool, con
 dsa_status_t mla_sparse_attn_decode_paged(const void *q, const void *kv_pool, const int32_t *kv_len,
                                           const int32_t *block_table, int bt_stride, int page_size,
                                           int num_pages, const int32_t *idx, int B, int Nmax,
-                                          int top_k, float scale, void *out, float *lse,
-                                          void *workspace, size_t ws_bytes, void *stream);
+                                          int top_k, float scale, void *out, int out_dtype,
+                                          float *lse, void *workspace, size_t ws_bytes,
+                                          void *stream);
 /* Prefill (a chunk of L queries of one sequence) over that sequence's paged
  * cache: mla_sparse_attn_prefill with kv[j] = kv_pool[block_table[j / page_size]
  * * page_size + j % page_size] for the N keys j < N (block_table holds
@@ -236,8 +260,8 @@ dsa_status_t mla_sparse_attn_decode_paged(const void *q, const void *kv_pool, co
 dsa_status_t mla_sparse_attn_prefill_paged(const void *q, const void *kv_pool,
                                            const int32_t *block_table, int page_size, int num_pages,
                                            const int32_t *idx, int L, int N, int top_k, float scale,
-                                           void *out, float *lse, void *workspace, size_t ws_bytes,
-                                           void *stream);
+                                           void *out, int out_dtype, float *lse, void *workspace,
+                                           size_t ws_bytes, void *stream);
 
 /*
  * mla_value_up_proj -- the value up-projection (wv_b) after the attention.

@@ -48,7 +48,7 @@ def test_exports_every_declared_symbol(lib):
 
 
 def test_version_and_strings(lib):
-    assert lib.dsa_abi_version() == 3
+    assert lib.dsa_abi_version() == 4
     for code in range(0, 10):
         s = lib.dsa_status_string(code)
         assert s and len(s) > 1
@@ -71,13 +71,15 @@ def test_host_validation_rejects_bad_arguments(lib):
     assert lib.dsa_topk(P, 16, P, P, 1, 1, 16, 2049, P, None, 0, stream) == 2
     assert lib.dsa_topk_workspace_size(1, 4096, 65536, 2048) == 0
     # attention
-    assert lib.mla_sparse_attn_prefill(P, P, P, 4, 64, 4096, 0.0625, P, None, None, 0, stream) == 2
-    assert lib.mla_sparse_attn_prefill(P, P, P, 4, 64, 32, -1.0, P, None, None, 0, stream) == 1
-    assert lib.mla_sparse_attn_prefill(P, P + 8, P, 4, 64, 32, 0.0625, P, None, None, 0, stream) == 3
+    assert lib.mla_sparse_attn_prefill(P, P, P, 4, 64, 4096, 0.0625, P, 0, None, None, 0, stream) == 2
+    assert lib.mla_sparse_attn_prefill(P, P, P, 4, 64, 32, -1.0, P, 0, None, None, 0, stream) == 1
+    assert lib.mla_sparse_attn_prefill(P, P + 8, P, 4, 64, 32, 0.0625, P, 0, None, None, 0, stream) == 3
+    assert lib.mla_sparse_attn_prefill(P, P, P, 4, 64, 32, 0.0625, P, 2, None, None, 0, stream) == 1  # out_dtype
     ws = lib.mla_sparse_attn_workspace_size(8, 1, 2048, 1)
     assert ws > 0 and lib.mla_sparse_attn_workspace_size(1, 4096, 2048, 0) == 0
-    assert lib.mla_sparse_attn_decode(P, P, P, P, 8, 4096, 2048, 0.0625, P, None, P, ws - 1, stream) == 4
-    assert lib.mla_sparse_attn_decode(P, P, P, P, 8, 4096, 2048, 0.0625, P, None, None, ws, stream) == 1
+    assert lib.mla_sparse_attn_decode(P, P, P, P, 8, 4096, 2048, 0.0625, P, 0, None, P, ws - 1, stream) == 4
+    assert lib.mla_sparse_attn_decode(P, P, P, P, 8, 4096, 2048, 0.0625, P, 1, None, None, ws, stream) == 1
+    assert lib.mla_sparse_attn_decode(P, P, P, P, 8, 4096, 2048, 0.0625, P, -1, None, P, ws, stream) == 1
     # paged caches: (block_table, bt_stride, page_size, num_pages) geometry
     idx_paged = lib.dsa_indexer_scores_paged
     assert idx_paged(P, P, P, P, P, None, 4, 64, 8, 1, 1, 256, P, 256, stream) == 1        # no table
@@ -87,15 +89,15 @@ def test_host_validation_rejects_bad_arguments(lib):
     assert idx_paged(P, P, P, P, P, P, 4, 65536, 1 << 16, 1, 1, 256, P, 256, stream) == 2  # pool rows > 2^31-1
     assert idx_paged(P, P + 2, P, P, P, P, 4, 64, 8, 1, 1, 256, P, 256, stream) == 3       # k_pool misaligned
     dec_paged = lib.mla_sparse_attn_decode_paged
-    assert dec_paged(P, P, P, P, 4, 64, 8, P, 8, 256, 2048, 0.0625, P, None, P, ws - 1, stream) == 4
-    assert dec_paged(P, P, P, P, 0, 64, 8, P, 8, 256, 2048, 0.0625, P, None, P, ws, stream) == 1
-    assert dec_paged(P, P, P, P, 4, 100, 8, P, 8, 256, 2048, 0.0625, P, None, P, ws, stream) == 2
-    assert dec_paged(P, P, P, P, 4, 64, 8, P, 8, 256, 0, 0.0625, P, None, P, ws, stream) == 2
+    assert dec_paged(P, P, P, P, 4, 64, 8, P, 8, 256, 2048, 0.0625, P, 0, None, P, ws - 1, stream) == 4
+    assert dec_paged(P, P, P, P, 0, 64, 8, P, 8, 256, 2048, 0.0625, P, 0, None, P, ws, stream) == 1
+    assert dec_paged(P, P, P, P, 4, 100, 8, P, 8, 256, 2048, 0.0625, P, 0, None, P, ws, stream) == 2
+    assert dec_paged(P, P, P, P, 4, 64, 8, P, 8, 256, 0, 0.0625, P, 0, None, P, ws, stream) == 2
     pre_paged = lib.mla_sparse_attn_prefill_paged
-    assert pre_paged(P, P, None, 64, 8, P, 4, 256, 32, 0.0625, P, None, None, 0, stream) == 1       # no table
-    assert pre_paged(P, P, P, 48, 8, P, 4, 256, 32, 0.0625, P, None, None, 0, stream) == 2         # page size
-    assert pre_paged(P, P, P, 64, 8, P, 4, 256, 4096, 0.0625, P, None, None, 0, stream) == 2       # top_k
-    assert pre_paged(P, P + 4, P, 64, 8, P, 4, 256, 32, 0.0625, P, None, None, 0, stream) == 3     # kv_pool
+    assert pre_paged(P, P, None, 64, 8, P, 4, 256, 32, 0.0625, P, 0, None, None, 0, stream) == 1       # no table
+    assert pre_paged(P, P, P, 48, 8, P, 4, 256, 32, 0.0625, P, 0, None, None, 0, stream) == 2         # page size
+    assert pre_paged(P, P, P, 64, 8, P, 4, 256, 4096, 0.0625, P, 0, None, None, 0, stream) == 2       # top_k
+    assert pre_paged(P, P + 4, P, 64, 8, P, 4, 256, 32, 0.0625, P, 0, None, None, 0, stream) == 3     # kv_pool
     # value up-projection
     assert lib.mla_value_up_proj(None, P, 4, P, stream) == 1
     assert lib.mla_value_up_proj(P, P, 0, P, stream) == 1

@@ -70,8 +70,22 @@ def test_reference_arm_prints_one_json_line():
     assert len(lines) == 1
     d = json.loads(lines[0])
     assert d["impl"] == "reference" and d["higher_is_better"] is True
-    assert d["metric"] == bench.METRIC and d["unit"] == bench.UNIT and d["value"] > 0
+    assert d["metric"] == bench.metric_name(bench.W.WORKLOADS["tiny_1k"]) and d["unit"] == bench.UNIT
+    assert d["value"] > 0
     assert d["config"]["workload"] == "tiny_1k" and d["n_gpus"] == 1
     assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] >= 1
     assert d["cpu_baseline"]["value"] == d["value"]
     assert d["e2e"] == {"value": d["value"], "unit": d["unit"], "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
+
+
+def test_each_workload_line_names_its_own_context():
+    """The headline (16k chunk) keeps the metric string of the benchmark contract; every other
+    line states its own context, so a 64k line never reads "16k ctx"."""
+    W = bench.W
+    assert bench.metric_name(W.WORKLOADS["prefill_16k"]) == bench.METRIC
+    assert "at 64k ctx" in bench.metric_name(W.WORKLOADS["prefill_64k"])
+    assert "at 4k ctx" in bench.metric_name(W.WORKLOADS["first_chunk_4k"])
+    assert "at 1k ctx" in bench.metric_name(W.WORKLOADS["tiny_1k"])
+    assert bench.metric_name(W.WORKLOADS["decode_b8"]).startswith("decode us/step")
+    names = {bench.metric_name(w) for w in W.WORKLOADS.values() if w.L > 1}
+    assert len(names) == len([w for w in W.WORKLOADS.values() if w.L > 1])

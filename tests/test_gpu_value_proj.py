@@ -110,7 +110,7 @@ def test_value_up_proj_after_attention_chain(dsa, oracle_mod):
     S = dsa.indexer_scores(dev(qi), dev(ki), torch.from_numpy(w).cuda(), torch.from_numpy(q_pos0).cuda(),
                            torch.from_numpy(kv_len).cuda())
     idx = dsa.topk(S, torch.from_numpy(q_pos0).cuda(), torch.from_numpy(kv_len).cuda(), wl.N, wl.top_k)
-    out = dsa.mla_sparse_attn_prefill(dev(q[0]), dev(kv[0]), idx[0], W.SCALE)
+    out = dsa.mla_sparse_attn_prefill(dev(q[0]), dev(kv[0]), idx[0], W.SCALE, out_dtype=torch.bfloat16)
     _, wv = W.make_value_proj_inputs(1, seed=2001)
     v = dsa.mla_value_up_proj(out, dev(wv))
     torch.cuda.synchronize()

@@ -42,9 +42,19 @@ def _close(got, ref):
     assert err.sum() / np.abs(ref).sum() <= 2e-3
 
 
-@pytest.mark.parametrize("name", ["decode_b8", "decode_b1"])
-def test_noalloc_decode_matches_workspace_decode_twice(dsa, name):
-    wl = W.WORKLOADS[name]
+def _bf16_bits(t):
+    return t.to(torch.bfloat16).view(torch.int16)
+
+
+# B = 63 fills the whole scratch (one split per sequence); B = 32 is the first batch where the
+# scratch, not the SM count, caps the splits at one per sequence.
+CASES = [W.WORKLOADS["decode_b8"], W.WORKLOADS["decode_b1"],
+         W.custom("decode_b63", B=63, L=1, p0=4095, N=4096, top_k=2048, seed=1063),
+         W.custom("decode_b32", B=32, L=1, p0=4095, N=4096, top_k=2048, seed=1032)]
+
+
+@pytest.mark.parametrize("wl", CASES, ids=lambda w: w.name)
+def test_noalloc_decode_matches_workspace_decode_twice(dsa, wl):
     qi, ki, w = W.make_indexer_inputs(wl)
     q, kv = W.make_attention_inputs(wl)
     q_pos0, kv_len = W.positions(wl)
@@ -62,10 +72,15 @@ def test_noalloc_decode_matches_workspace_decode_twice(dsa, name):
         torch.cuda.synchronize()
         _close(out, ref)
         np.testing.assert_allclose(lse.cpu().numpy(), ref_lse.cpu().numpy(), rtol=1e-5, atol=1e-5)
+    # the bf16 output is the float32 result rounded to nearest even
+    out16 = dsa.mla_sparse_attn_decode_noalloc(dq, dkv, d_len, idx, W.SCALE, out_dtype=torch.bfloat16)
+    again = dsa.mla_sparse_attn_decode_noalloc(dq, dkv, d_len, idx, W.SCALE)
+    torch.cuda.synchronize()
+    assert torch.equal(out16.view(torch.int16), _bf16_bits(again))
     assert dsa.device_status() == 0
 
 
 def test_noalloc_rejects_batches_beyond_the_scratch(dsa):
     P = torch.empty(16, dtype=torch.uint8, device="cuda").data_ptr()
-    rc = dsa.load().mla_sparse_attn_decode_noalloc(P, P, P, P, 64, 4096, 2048, 0.0625, P, None, None)
+    rc = dsa.load().mla_sparse_attn_decode_noalloc(P, P, P, P, 64, 4096, 2048, 0.0625, P, 0, None, None)
     assert rc == 9        # DSA_ERR_SCRATCH_TOO_SMALL, nothing launched
