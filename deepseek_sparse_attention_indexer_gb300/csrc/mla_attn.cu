@@ -88,8 +88,8 @@ constexpr int OFF_MUSED = OFF_RED + 4 * kH * 4;        // float [64]
 constexpr int OFF_ALPHA = OFF_MUSED + kH * 4;          // float [64]
 constexpr int OFF_INVL = OFF_ALPHA + kH * 4;           // float [64]
 constexpr int OFF_BAR = OFF_INVL + kH * 4;
-// barriers: q_full, q_empty, seg_full[5], seg_free[4], s_full, s_empty, p_full, pv_done
-constexpr int N_BARS = 2 + 5 + kSegs + 4;
+// barriers: q_full, q_empty, seg_full[5], seg_free[4], s_full, p_full
+constexpr int N_BARS = 2 + 5 + kSegs + 2;
 constexpr int OFF_TMEM = OFF_BAR + N_BARS * 8;
 constexpr int OFF_ABORT = OFF_TMEM + 4;
 constexpr int SMEM_BYTES = OFF_ABORT + 4 + 1024;
@@ -217,9 +217,7 @@ __global__ void __launch_bounds__(kThreads, 1)   // 18 warps: at most 96 registe
     uint64_t* seg_full = bars + 2;
     uint64_t* seg_free = bars + 7;   // latent chunk c (blocks 2c, 2c+1; chunk 3 also the rope block) consumed by PV
     uint64_t* s_full = bars + 7 + kSegs;
-    uint64_t* s_empty = s_full + 1;
-    uint64_t* p_full = s_full + 2;
-    uint64_t* pv_done = s_full + 3;
+    uint64_t* p_full = s_full + 1;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + OFF_TMEM);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + OFF_ABORT);
 
@@ -232,9 +230,7 @@ __global__ void __launch_bounds__(kThreads, 1)   // 18 warps: at most 96 registe
         for (int c = 0; c < 5; ++c) mbar_init(&seg_full[c], kWorkers);  // one cp.async arrival per worker thread
         for (int c = 0; c < kSegs; ++c) mbar_init(&seg_free[c], 1);
         mbar_init(s_full, 1);
-        mbar_init(s_empty, kWorkerWarps);
         mbar_init(p_full, kWorkerWarps);
-        mbar_init(pv_done, 1);
         *abort_flag = 0;
         fence_mbar_init();
         tma_prefetch_desc(&tmap_q);
@@ -281,8 +277,10 @@ __global__ void __launch_bounds__(kThreads, 1)   // 18 warps: at most 96 registe
                 const uint32_t kv_base = smem_u32(sKV);
                 bool q_released = false;
                 for (int t = 0; ok && t < T; ++t, ++gt) {
-                    // ---- S^T = K . Q^T over the 576 dims, segment by segment
-                    if (!(ok = mbar_wait_spin(s_empty, (gt & 1) ^ 1, abort_flag, p.status))) break;
+                    // ---- S^T = K . Q^T over the 576 dims, segment by segment as the copies land.
+                    // The S^T accumulator needs no wait of its own: the previous tile's
+                    // probabilities (p_full, awaited before its PV) were written after every
+                    // worker had read S^T.
                     for (int c = 0; c < 5 && ok; ++c) {
                         if (!(ok = mbar_wait_spin(&seg_full[c], gt & 1, abort_flag, p.status))) break;
                         tc_fence_after();
@@ -320,9 +318,10 @@ __global__ void __launch_bounds__(kThreads, 1)   // 18 warps: at most 96 registe
                             const uint64_t bd = sdesc_sw128(p_base + kk * 2048, kBlkBytes, 1024);
                             mma_bf16_ss(tmem_base + TM_O + 64 * c, ad, bd, IDESC_PV, (t > 0 || kk > 0) ? 1u : 0u);
                         }
-                        mma_commit(&seg_free[c]);   // chunk 3 is the last reader of P^T: frees the rope block too
+                        // chunk 3 is the last reader of P^T: its commit also frees the rope block and
+                        // tells the workers that this tile's PV is complete
+                        mma_commit(&seg_free[c]);
                     }
-                    mma_commit(pv_done);
                 }
                 if (ok && !q_released) mma_commit(q_empty);
                 ++qi;
@@ -474,8 +473,6 @@ __global__ void __launch_bounds__(kThreads, 1)   // 18 warps: at most 96 registe
                     for (int h = 0; h < kHG; ++h) x[h] = __uint_as_float(v[h]);
                 }
                 tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(s_empty);
                 const bool kvalid = (j >= 0) && (j < I.bound);
                 // Reference maxima (scaled, log2 units), one per head: set from the item's
                 // first tile, afterwards moved only when a score exceeds its head's reference
@@ -559,7 +556,7 @@ __global__ void __launch_bounds__(kThreads, 1)   // 18 warps: at most 96 registe
                 fence_proxy_async_smem();
                 if (any_upd && t > 0) {
                     // O^T columns of the raised heads: wait for the previous PV, then rescale in TMEM
-                    gok = gok && worker_wait(pv_done, (gt - 1) & 1, abort_flag, p.status);
+                    gok = gok && worker_wait(&seg_free[kSegs - 1], (gt - 1) & 1, abort_flag, p.status);
                     tc_fence_after();
 #pragma unroll 1
                     for (int c = 0; c < 4; ++c) {
@@ -585,7 +582,7 @@ __global__ void __launch_bounds__(kThreads, 1)   // 18 warps: at most 96 registe
                 if ((lane & 1u) == 0) red[quad * kH + h0 + (int)(lane >> 1)] = r;
             }
             if (!named_bar_and(2, kWorkers,
-                               gok && (T == 0 || worker_wait(pv_done, (gt - 1) & 1, abort_flag, p.status)))) {
+                               gok && (T == 0 || worker_wait(&seg_free[kSegs - 1], (gt - 1) & 1, abort_flag, p.status)))) {
                 failed = true;
                 break;
             }
