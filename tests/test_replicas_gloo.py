@@ -39,7 +39,7 @@ def _rank_main(rank, world, port, results):
 def test_two_gloo_ranks_take_the_slowest_rank():
     world = 2
     port = _free_port()
-    results = mp.Manager().dict()
+    results = mp.get_context("spawn").Manager().dict()   # no fork once CUDA may be initialised
     mp.spawn(_rank_main, args=(world, port, results), nprocs=world, join=True)
     for rank in range(world):
         slowest, rate, rc = results[rank]
