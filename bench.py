@@ -427,6 +427,22 @@ def run_gpu(args, wl, rank, world, local_rank):
 
         def e2e_step():
             runner(*host_in, host_out, W.SCALE, stream=stream)
+    elif decode and not wl.page_size:
+        # the package's decode step: uploads of the new tokens' inputs, the calls and the download,
+        # replayed as one CUDA graph over device-resident caches
+        from deepseek_sparse_attention_indexer_gb300.host_decode import HostDecode
+        runner = HostDecode(dev_in[1], dev_in[6], wl.top_k, W.SCALE, out_dtype=out.dtype)
+        runner.h_qi.copy_(host_in[0].view(torch.int16))
+        runner.h_w.copy_(host_in[2])
+        runner.h_pos.copy_(host_in[3])
+        runner.h_len.copy_(host_in[4])
+        runner.h_q.copy_(host_in[5].view(torch.int16)[:, 0])
+        e2e_api = ("HostDecode: H2D of the new tokens' inputs (caches resident), the calls and D2H of the "
+                   "output, replayed as one CUDA graph")
+        h2d, d2h = runner.h2d_bytes, runner.d2h_bytes
+
+        def e2e_step():
+            runner(stream=stream)
     else:
         e2e_api = ("H2D of the new tokens' inputs (caches resident), the calls, D2H of the output, in stream "
                    "order" if decode else "H2D of every input, the calls, D2H of the output, in stream order")

@@ -9,7 +9,9 @@ torch CUDA tensors into device pointers and the current stream.
         mla_sparse_attn_prefill, mla_sparse_attn_decode
 
 HostPrefill runs a prefill chunk from pinned host buffers with the copies
-overlapped with the kernels (see host_prefill.py).
+overlapped with the kernels (see host_prefill.py); HostDecode replays a batched
+decode step -- uploads, the library calls and the download -- as one CUDA graph
+(see host_decode.py).
 """
 
 _API = ("indexer_scores", "topk", "mla_sparse_attn_prefill", "mla_sparse_attn_decode",
@@ -17,7 +19,7 @@ _API = ("indexer_scores", "topk", "mla_sparse_attn_prefill", "mla_sparse_attn_de
         "mla_sparse_attn_prefill_paged", "mla_value_up_proj", "indexer_source_layer",
         "attn_workspace_size", "device_status", "status_string", "load", "lib_path", "DsaError")
 
-__all__ = list(_API) + ["workloads", "build", "HostPrefill"]
+__all__ = list(_API) + ["workloads", "build", "HostPrefill", "HostDecode", "sharding"]
 
 
 def __getattr__(name):
@@ -31,4 +33,10 @@ def __getattr__(name):
     if name == "HostPrefill":
         from .host_prefill import HostPrefill
         return HostPrefill
+    if name == "HostDecode":
+        from .host_decode import HostDecode
+        return HostDecode
+    if name in ("workloads", "sharding"):
+        import importlib
+        return importlib.import_module("." + name, __name__)
     raise AttributeError(name)

@@ -585,3 +585,38 @@ def test_chain_128k_keys(dsa, oracle_mod):
     attn_close(out.float().cpu().numpy(), o_ref, wl.name)
     np.testing.assert_allclose(lse.cpu().numpy(), l_ref, rtol=1e-5, atol=1e-5)
     assert dsa.device_status() == 0
+
+
+def test_host_decode_graph_replays_match_device_calls(dsa):
+    """HostDecode (uploads of the new tokens' inputs, the three calls and the download captured once
+    and replayed as a CUDA graph) gives the same bits as the device calls, step after step, when the
+    caller changes the pinned inputs between steps."""
+    from deepseek_sparse_attention_indexer_gb300.host_decode import HostDecode
+    wl = W.custom("host_decode", B=6, L=1, p0=0, N=3000, top_k=1024, seed=91)
+    qi, ki, w = W.make_indexer_inputs(wl)
+    q, kv = W.make_attention_inputs(wl)
+    rng = np.random.default_rng(92)
+    kv_len = rng.integers(1, wl.N + 1, size=wl.B).astype(np.int32)
+    kv_len[0] = wl.N
+    q_pos0 = kv_len - 1
+    d_ki, d_kv = dev(ki), dev(kv)
+    runner = HostDecode(d_ki, d_kv, wl.top_k, W.SCALE)
+    for step in range(3):
+        # a different "new token" each step: reseeded indexer query, weights and absorbed query
+        qi_s = np.roll(qi, step, axis=0)
+        w_s = np.roll(w, step, axis=0)
+        q_s = np.roll(q, step, axis=0)
+        runner.h_qi.copy_(torch.from_numpy(qi_s.view(np.int16)))
+        runner.h_w.copy_(torch.from_numpy(w_s))
+        runner.h_q.copy_(torch.from_numpy(np.ascontiguousarray(q_s[:, 0]).view(np.int16)))
+        runner.h_pos.copy_(torch.from_numpy(q_pos0))
+        runner.h_len.copy_(torch.from_numpy(kv_len))
+        h_out = runner()
+        torch.cuda.synchronize()
+        S = dsa.indexer_scores(dev(qi_s), d_ki, dev(w_s), dev(q_pos0), dev(kv_len))
+        idx = dsa.topk(S, dev(q_pos0), dev(kv_len), wl.N, wl.top_k)
+        ref = dsa.mla_sparse_attn_decode(dev(np.ascontiguousarray(q_s[:, 0])), d_kv, dev(kv_len), idx[:, 0].contiguous(),
+                                         W.SCALE)
+        torch.cuda.synchronize()
+        assert torch.equal(h_out, ref.cpu()), f"step {step}"
+    assert dsa.device_status() == 0
