@@ -571,6 +571,37 @@ def test_host_prefill_matches_device_calls(dsa, L, slices, out_dtype):
     assert dsa.device_status() == 0
 
 
+def test_host_prefill_two_sets_overlaps_consecutive_chunks(dsa):
+    """HostPrefill with two device buffer sets: three consecutive chunks with different inputs are
+    enqueued back to back (the next chunk's uploads and kernels under the previous chunk's
+    download), each into its own pinned output, with no synchronisation between them; each output
+    holds the same bits as the device calls on that chunk's inputs."""
+    from deepseek_sparse_attention_indexer_gb300.host_prefill import HostPrefill
+    pin = lambda a: torch.from_numpy(np.ascontiguousarray(a.view(np.int16) if a.dtype == np.uint16 else a)).pin_memory()
+    L, p0, top_k = 400, 1700, 512
+    runner = HostPrefill(L, p0 + L, top_k, slices=3, sets=2)
+    chunks, outs, events = [], [], []
+    for c in range(3):
+        wl = W.custom(f"host_sets_{c}", B=1, L=L, p0=p0, N=p0 + L, top_k=top_k, seed=131 + c)
+        qi, ki, w = W.make_indexer_inputs(wl)
+        q, kv = W.make_attention_inputs(wl)
+        q_pos0, kv_len = W.positions(wl)
+        chunks.append((wl, qi, ki, w, q_pos0, kv_len, q, kv))
+        outs.append(torch.full((L, 64, 512), float("nan"), dtype=torch.float32).pin_memory())
+    hosts = [[pin(a) for a in ch[1:]] for ch in chunks]
+    for c in range(3):
+        events.append(runner(*hosts[c], outs[c], W.SCALE))
+    for e in events:
+        e.synchronize()
+    for c, (wl, qi, ki, w, q_pos0, kv_len, q, kv) in enumerate(chunks):
+        S = dsa.indexer_scores(dev(qi), dev(ki), dev(w), dev(q_pos0), dev(kv_len))
+        idx = dsa.topk(S, dev(q_pos0), dev(kv_len), wl.N, top_k)
+        ref = dsa.mla_sparse_attn_prefill(dev(q[0]), dev(kv[0]), idx[0], W.SCALE)
+        torch.cuda.synchronize()
+        assert torch.equal(outs[c], ref.cpu()), f"chunk {c}"
+    assert dsa.device_status() == 0
+
+
 def test_chain_128k_keys(dsa, oracle_mod):
     """Beyond the configs: 16 queries at the end of a 131072-key context (the streaming top-k, 1024
     key tiles per indexer query group), every output checked."""
