@@ -73,7 +73,8 @@ constexpr int kBlkBytes = kTile * 128; // 16 KB: 128 keys x 64 dims
 constexpr int kQBlkBytes = kH * 128;   // 8 KB: 64 heads x 64 dims
 constexpr int kWorkerWarps = 16;                  // gather + softmax warps
 constexpr int kWorkers = kWorkerWarps * 32;        // 512
-constexpr int kThreads = 64 + kWorkers;            // warp 0 Q loader, warp 1 MMA, warps 2.. workers
+constexpr int kIssuers = 2;                        // MMA-issuing warps
+constexpr int kThreads = 32 * (1 + kIssuers) + kWorkers;  // warp 0 Q loader, warps 1-2 MMA, warps 3.. workers
 constexpr int kHG = kH / (kWorkerWarps / 4);       // 16 heads per worker warp
 constexpr int kGroupThreads = 4 * 32;              // the four warps sharing a head group
 constexpr int kSegs = 4;               // PV releases the stage by 128-dim latent chunk (the rope block with the last)
@@ -95,8 +96,8 @@ constexpr int OFF_ABORT = OFF_TMEM + 4;
 constexpr int SMEM_BYTES = OFF_ABORT + 4 + 1024;
 
 constexpr uint32_t TMEM_COLS = 512;
-constexpr uint32_t TM_S = 0;      // S^T: 64 columns
-constexpr uint32_t TM_O = 64;     // O^T chunk c at 64 + 64 c
+constexpr uint32_t TM_S = 0;      // S^T partial sums: issuer i's 64 columns at 64 i
+constexpr uint32_t TM_O = 128;    // O^T chunk c at 128 + 64 c
 
 constexpr uint32_t IDESC_QK = idesc_bf16_f32(128, 64, false, false);
 constexpr uint32_t IDESC_PV = idesc_bf16_f32(128, 64, true, true);
@@ -201,7 +202,7 @@ __device__ __forceinline__ float warp_transpose_reduce16(const float (&x)[16], u
 }
 
 template <bool PARTIAL, bool PAGED>
-__global__ void __launch_bounds__(kThreads, 1)   // 18 warps: at most 96 registers a thread (5 warps share one 16K-register SM sub-partition)
+__global__ void __launch_bounds__(kThreads, 1)   // 19 warps: at most 96 registers a thread (5 warps share one 16K-register SM sub-partition)
     mla_sparse_attn_kernel(const __grid_constant__ CUtensorMap tmap_q, const AttnParams p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -226,10 +227,10 @@ __global__ void __launch_bounds__(kThreads, 1)   // 18 warps: at most 96 registe
 
     if (threadIdx.x == 0) {
         mbar_init(q_full, 1);
-        mbar_init(q_empty, 1);
+        mbar_init(q_empty, kIssuers);   // both issuers' last QK of an item read Q^T
         for (int c = 0; c < 5; ++c) mbar_init(&seg_full[c], kWorkers);  // one cp.async arrival per worker thread
         for (int c = 0; c < kSegs; ++c) mbar_init(&seg_free[c], 1);
-        mbar_init(s_full, 1);
+        mbar_init(s_full, kIssuers);    // both partial sums of S^T
         mbar_init(p_full, kWorkerWarps);
         *abort_flag = 0;
         fence_mbar_init();
@@ -261,8 +262,16 @@ __global__ void __launch_bounds__(kThreads, 1)   // 18 warps: at most 96 registe
                 for (int b = 0; b < 9; ++b) tma_load_2d(sQ + b * kQBlkBytes, &tmap_q, q_full, b * 64, qrow);
             }
         }
-    } else if (warp == 1) {
-        // ------------------------------------------------------------ MMA issuer
+    } else if (warp <= kIssuers) {
+        // ------------------------------------------------------------ MMA issuers
+        // A single issuing thread keeps the tensor core at one M128 N64 K16 MMA per ~70 cycles;
+        // two independent issuers reach one per ~48.  The work splits by latent chunk: issuer 0
+        // takes QK over chunks 0-1 (dims 0..255) into its own S^T partial sum and PV for O^T
+        // chunks 0-1; issuer 1 takes QK over chunks 2-3 and the rope block (dims 256..575) and PV
+        // for O^T chunks 2-3.  The softmax adds the two partial sums.
+        const int iss = warp - 1;
+        const int seg_lo = iss == 0 ? 0 : 2, seg_hi = iss == 0 ? 2 : 5;   // QK segments [lo, hi)
+        const uint32_t tm_s = tmem_base + TM_S + 64 * (uint32_t)iss;
         int gt = 0, qi = 0;
         bool ok = true;
         for (int s = 0; ok; ++s) {
@@ -277,11 +286,11 @@ __global__ void __launch_bounds__(kThreads, 1)   // 18 warps: at most 96 registe
                 const uint32_t kv_base = smem_u32(sKV);
                 bool q_released = false;
                 for (int t = 0; ok && t < T; ++t, ++gt) {
-                    // ---- S^T = K . Q^T over the 576 dims, segment by segment as the copies land.
-                    // The S^T accumulator needs no wait of its own: the previous tile's
+                    // ---- this issuer's part of S^T = K . Q^T, segment by segment as the copies
+                    // land.  Its accumulator needs no wait of its own: the previous tile's
                     // probabilities (p_full, awaited before its PV) were written after every
-                    // worker had read S^T.
-                    for (int c = 0; c < 5 && ok; ++c) {
+                    // worker had read both partial sums.
+                    for (int c = seg_lo; c < seg_hi && ok; ++c) {
                         if (!(ok = mbar_wait_spin(&seg_full[c], gt & 1, abort_flag, p.status))) break;
                         tc_fence_after();
                         const int b_lo = (c < 4) ? 2 * c : 8;
@@ -292,7 +301,7 @@ __global__ void __launch_bounds__(kThreads, 1)   // 18 warps: at most 96 registe
                             for (int kk = 0; kk < 4; ++kk) {
                                 const uint64_t ad = sdesc_sw128(kv_base + blk * kBlkBytes + kk * 32, 16, 1024);
                                 const uint64_t bd = sdesc_sw128(q_base + blk * kQBlkBytes + kk * 32, 16, 1024);
-                                mma_bf16_ss(tmem_base + TM_S, ad, bd, IDESC_QK, (c | bb | kk) != 0);
+                                mma_bf16_ss(tm_s, ad, bd, IDESC_QK, (c != seg_lo || bb | kk) ? 1u : 0u);
                             }
                         }
                     }
@@ -302,14 +311,15 @@ __global__ void __launch_bounds__(kThreads, 1)   // 18 warps: at most 96 registe
                         mma_commit(q_empty);  // the next query's Q^T may stream in during the last softmax
                         q_released = true;
                     }
-                    // ---- O^T += V^T . P^T, one 128-dim latent chunk at a time: each chunk's
-                    // blocks are freed as soon as it is consumed, so the next tile's copies
-                    // of that chunk (and then its QK) overlap the rest of this PV
+                    // ---- O^T += V^T . P^T for this issuer's two 128-dim latent chunks: each
+                    // chunk's blocks are freed as soon as it is consumed, so the next tile's
+                    // copies of that chunk (and then its QK) overlap the rest of this PV
                     if (!(ok = mbar_wait_spin(p_full, gt & 1, abort_flag, p.status))) break;
                     tc_fence_after();
                     const uint32_t p_base = kv_base + 8 * kBlkBytes;
 #pragma unroll
-                    for (int c = 0; c < kSegs; ++c) {
+                    for (int cc = 0; cc < 2; ++cc) {
+                        const int c = 2 * iss + cc;
 #pragma unroll
                         for (int kk = 0; kk < 8; ++kk) {   // 16 keys per K step
                             // A = V^T: MN-major, 64-dim atoms 16 KB apart (LBO), 8-key groups 1 KB apart (SBO)
@@ -318,8 +328,8 @@ __global__ void __launch_bounds__(kThreads, 1)   // 18 warps: at most 96 registe
                             const uint64_t bd = sdesc_sw128(p_base + kk * 2048, kBlkBytes, 1024);
                             mma_bf16_ss(tmem_base + TM_O + 64 * c, ad, bd, IDESC_PV, (t > 0 || kk > 0) ? 1u : 0u);
                         }
-                        // chunk 3 is the last reader of P^T: its commit also frees the rope block and
-                        // tells the workers that this tile's PV is complete
+                        // seg_free[1] and seg_free[3] each end one issuer's reads of P^T for this
+                        // tile; the copies of the rope block (which P^T overwrites) wait for both
                         mma_commit(&seg_free[c]);
                     }
                 }
@@ -329,8 +339,8 @@ __global__ void __launch_bounds__(kThreads, 1)   // 18 warps: at most 96 registe
             ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
         }
     } else {
-        // ------------------------------------------------------------ workers (warps 2..17)
-        const int ww = warp - 2;                  // 0..15
+        // ------------------------------------------------------------ workers (warps 3..18)
+        const int ww = warp - 1 - kIssuers;       // 0..15
         const int quad = warp & 3;                // TMEM lane quadrant this warp may access
         const int hg = ww >> 2;                   // head group: heads h0 .. h0 + 15
         const int h0 = hg * kHG;
@@ -423,7 +433,7 @@ __global__ void __launch_bounds__(kThreads, 1)   // 18 warps: at most 96 registe
                         cp_async_16(kv_smem + blk * kBlkBytes + off_h[h], src_h[h] + blk * 128, nbytes_h[h]);
                 }
                 cp_async_arrive_noinc(&seg_full[c]);
-                if (c == kSegs - 1) {   // the rope block: P^T's last reader (PV chunk 3) is done
+                if (c == kSegs - 1) {   // the rope block: P^T's readers (PV chunks 1 and 3, waited above) are done
 #pragma unroll
                     for (int h = 0; h < 2; ++h)
                         cp_async_16(kv_smem + 8 * kBlkBytes + off_h[h], src_h[h] + 8 * 128, nbytes_h[h]);
@@ -466,11 +476,12 @@ __global__ void __launch_bounds__(kThreads, 1)   // 18 warps: at most 96 registe
                 tc_fence_after();
                 float x[kHG];
                 {
-                    uint32_t v[kHG];
-                    tmem_ld16(tmem_base + lane_addr + TM_S + h0, v);
+                    uint32_t v[kHG], u[kHG];
+                    tmem_ld16(tmem_base + lane_addr + TM_S + h0, v);        // dims 0..255
+                    tmem_ld16(tmem_base + lane_addr + TM_S + 64 + h0, u);   // dims 256..575
                     tmem_ld_wait();
 #pragma unroll
-                    for (int h = 0; h < kHG; ++h) x[h] = __uint_as_float(v[h]);
+                    for (int h = 0; h < kHG; ++h) x[h] = __uint_as_float(v[h]) + __uint_as_float(u[h]);
                 }
                 tc_fence_before();
                 const bool kvalid = (j >= 0) && (j < I.bound);
@@ -555,8 +566,10 @@ __global__ void __launch_bounds__(kThreads, 1)   // 18 warps: at most 96 registe
                 }
                 fence_proxy_async_smem();
                 if (any_upd && t > 0) {
-                    // O^T columns of the raised heads: wait for the previous PV, then rescale in TMEM
-                    gok = gok && worker_wait(&seg_free[kSegs - 1], (gt - 1) & 1, abort_flag, p.status);
+                    // O^T columns of the raised heads: wait for the previous PV (both issuers'
+                    // halves), then rescale in TMEM
+                    gok = gok && worker_wait(&seg_free[1], (gt - 1) & 1, abort_flag, p.status) &&
+                          worker_wait(&seg_free[kSegs - 1], (gt - 1) & 1, abort_flag, p.status);
                     tc_fence_after();
 #pragma unroll 1
                     for (int c = 0; c < 4; ++c) {
@@ -582,7 +595,8 @@ __global__ void __launch_bounds__(kThreads, 1)   // 18 warps: at most 96 registe
                 if ((lane & 1u) == 0) red[quad * kH + h0 + (int)(lane >> 1)] = r;
             }
             if (!named_bar_and(2, kWorkers,
-                               gok && (T == 0 || worker_wait(&seg_free[kSegs - 1], (gt - 1) & 1, abort_flag, p.status)))) {
+                               gok && (T == 0 || (worker_wait(&seg_free[1], (gt - 1) & 1, abort_flag, p.status) &&
+                                                  worker_wait(&seg_free[kSegs - 1], (gt - 1) & 1, abort_flag, p.status))))) {
                 failed = true;
                 break;
             }
