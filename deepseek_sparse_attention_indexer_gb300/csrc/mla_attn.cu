@@ -74,6 +74,11 @@ constexpr int kQBlkBytes = kH * 128;   // 8 KB: 64 heads x 64 dims
 constexpr int kWorkerWarps = 16;                  // gather + softmax warps
 constexpr int kWorkers = kWorkerWarps * 32;        // 512
 constexpr int kIssuers = 2;                        // MMA-issuing warps
+// issuer that owns latent chunk c (its QK segment and its PV); the rope block goes with chunk 3.
+// Interleaved, so that PV frees chunks 0 and 1 first, together, and the next tile's copies of
+// them (issued in chunk order) start as early as they can.
+__host__ __device__ constexpr int chunk_owner(int c) { return c % kIssuers; }
+constexpr int kMaxRegs = 96;                       // 19 warps: 5 share one 16K-register sub-partition
 constexpr int kThreads = 32 * (1 + kIssuers) + kWorkers;  // warp 0 Q loader, warps 1-2 MMA, warps 3.. workers
 constexpr int kHG = kH / (kWorkerWarps / 4);       // 16 heads per worker warp
 constexpr int kGroupThreads = 4 * 32;              // the four warps sharing a head group
@@ -96,8 +101,9 @@ constexpr int OFF_ABORT = OFF_TMEM + 4;
 constexpr int SMEM_BYTES = OFF_ABORT + 4 + 1024;
 
 constexpr uint32_t TMEM_COLS = 512;
-constexpr uint32_t TM_S = 0;      // S^T partial sums: issuer i's 64 columns at 64 i
-constexpr uint32_t TM_O = 128;    // O^T chunk c at 128 + 64 c
+constexpr uint32_t TM_S = 0;                       // S^T partial sums: issuer i's 64 columns at 64 i
+constexpr uint32_t TM_O = 64 * kIssuers;           // O^T chunk c at TM_O + 64 c
+static_assert(TM_O + 4 * 64 <= 512, "tensor memory columns");
 
 constexpr uint32_t IDESC_QK = idesc_bf16_f32(128, 64, false, false);
 constexpr uint32_t IDESC_PV = idesc_bf16_f32(128, 64, true, true);
@@ -202,7 +208,7 @@ __device__ __forceinline__ float warp_transpose_reduce16(const float (&x)[16], u
 }
 
 template <bool PARTIAL, bool PAGED>
-__global__ void __launch_bounds__(kThreads, 1)   // 19 warps: at most 96 registers a thread (5 warps share one 16K-register SM sub-partition)
+__global__ void __maxnreg__(kMaxRegs)   // kThreads threads, one CTA per SM
     mla_sparse_attn_kernel(const __grid_constant__ CUtensorMap tmap_q, const AttnParams p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -265,12 +271,11 @@ __global__ void __launch_bounds__(kThreads, 1)   // 19 warps: at most 96 registe
     } else if (warp <= kIssuers) {
         // ------------------------------------------------------------ MMA issuers
         // A single issuing thread keeps the tensor core at one M128 N64 K16 MMA per ~70 cycles;
-        // two independent issuers reach one per ~48.  The work splits by latent chunk: issuer 0
-        // takes QK over chunks 0-1 (dims 0..255) into its own S^T partial sum and PV for O^T
-        // chunks 0-1; issuer 1 takes QK over chunks 2-3 and the rope block (dims 256..575) and PV
-        // for O^T chunks 2-3.  The softmax adds the two partial sums.
+        // two independent issuers reach one per ~48 (four are no faster).  The work splits by
+        // 128-dim latent chunk: issuer 0 owns chunks 0 and 2, issuer 1 chunks 1 and 3 and the
+        // rope block.  The owner of a chunk runs the QK over its dims into its own S^T partial
+        // sum and the PV for that O^T chunk; the softmax adds the two partial sums.
         const int iss = warp - 1;
-        const int seg_lo = iss == 0 ? 0 : 2, seg_hi = iss == 0 ? 2 : 5;   // QK segments [lo, hi)
         const uint32_t tm_s = tmem_base + TM_S + 64 * (uint32_t)iss;
         int gt = 0, qi = 0;
         bool ok = true;
@@ -290,7 +295,9 @@ __global__ void __launch_bounds__(kThreads, 1)   // 19 warps: at most 96 registe
                     // land.  Its accumulator needs no wait of its own: the previous tile's
                     // probabilities (p_full, awaited before its PV) were written after every
                     // worker had read both partial sums.
-                    for (int c = seg_lo; c < seg_hi && ok; ++c) {
+                    bool first = true;
+                    for (int c = 0; c < 5 && ok; ++c) {
+                        if (chunk_owner(c < 4 ? c : 3) != iss) continue;
                         if (!(ok = mbar_wait_spin(&seg_full[c], gt & 1, abort_flag, p.status))) break;
                         tc_fence_after();
                         const int b_lo = (c < 4) ? 2 * c : 8;
@@ -301,7 +308,8 @@ __global__ void __launch_bounds__(kThreads, 1)   // 19 warps: at most 96 registe
                             for (int kk = 0; kk < 4; ++kk) {
                                 const uint64_t ad = sdesc_sw128(kv_base + blk * kBlkBytes + kk * 32, 16, 1024);
                                 const uint64_t bd = sdesc_sw128(q_base + blk * kQBlkBytes + kk * 32, 16, 1024);
-                                mma_bf16_ss(tm_s, ad, bd, IDESC_QK, (c != seg_lo || bb | kk) ? 1u : 0u);
+                                mma_bf16_ss(tm_s, ad, bd, IDESC_QK, first ? 0u : 1u);
+                                first = false;
                             }
                         }
                     }
@@ -311,15 +319,15 @@ __global__ void __launch_bounds__(kThreads, 1)   // 19 warps: at most 96 registe
                         mma_commit(q_empty);  // the next query's Q^T may stream in during the last softmax
                         q_released = true;
                     }
-                    // ---- O^T += V^T . P^T for this issuer's two 128-dim latent chunks: each
+                    // ---- O^T += V^T . P^T for this issuer's 128-dim latent chunks: each
                     // chunk's blocks are freed as soon as it is consumed, so the next tile's
                     // copies of that chunk (and then its QK) overlap the rest of this PV
                     if (!(ok = mbar_wait_spin(p_full, gt & 1, abort_flag, p.status))) break;
                     tc_fence_after();
                     const uint32_t p_base = kv_base + 8 * kBlkBytes;
 #pragma unroll
-                    for (int cc = 0; cc < 2; ++cc) {
-                        const int c = 2 * iss + cc;
+                    for (int c = 0; c < 4; ++c) {
+                        if (chunk_owner(c) != iss) continue;
 #pragma unroll
                         for (int kk = 0; kk < 8; ++kk) {   // 16 keys per K step
                             // A = V^T: MN-major, 64-dim atoms 16 KB apart (LBO), 8-key groups 1 KB apart (SBO)
@@ -328,8 +336,8 @@ __global__ void __launch_bounds__(kThreads, 1)   // 19 warps: at most 96 registe
                             const uint64_t bd = sdesc_sw128(p_base + kk * 2048, kBlkBytes, 1024);
                             mma_bf16_ss(tmem_base + TM_O + 64 * c, ad, bd, IDESC_PV, (t > 0 || kk > 0) ? 1u : 0u);
                         }
-                        // seg_free[1] and seg_free[3] each end one issuer's reads of P^T for this
-                        // tile; the copies of the rope block (which P^T overwrites) wait for both
+                        // the copies of the rope block (which P^T overwrites) come after every
+                        // chunk's free, so after every issuer's reads of P^T
                         mma_commit(&seg_free[c]);
                     }
                 }
@@ -352,6 +360,11 @@ __global__ void __launch_bounds__(kThreads, 1)   // 19 warps: at most 96 registe
         uint8_t* pT = sKV + 8 * kBlkBytes;
         const uint8_t* kv_bytes = reinterpret_cast<const uint8_t*>(p.kv);
         const uint32_t kv_smem = smem_u32(sKV);
+        // PV of global tile g is complete once each issuer's last chunk (2 and 3) is free
+        auto pv_done = [&](int g) -> bool {
+            return worker_wait(&seg_free[kSegs - 2], g & 1, abort_flag, p.status) &&
+                   worker_wait(&seg_free[kSegs - 1], g & 1, abort_flag, p.status);
+        };
 
         // Gather cursor: walks this CTA's (item, tile) sequence one tile ahead
         // of the softmax.  Items without tiles are skipped here.  A worker warp
@@ -433,7 +446,7 @@ __global__ void __launch_bounds__(kThreads, 1)   // 19 warps: at most 96 registe
                         cp_async_16(kv_smem + blk * kBlkBytes + off_h[h], src_h[h] + blk * 128, nbytes_h[h]);
                 }
                 cp_async_arrive_noinc(&seg_full[c]);
-                if (c == kSegs - 1) {   // the rope block: P^T's readers (PV chunks 1 and 3, waited above) are done
+                if (c == kSegs - 1) {   // the rope block: every chunk is free, so both issuers' reads of P^T are done
 #pragma unroll
                     for (int h = 0; h < 2; ++h)
                         cp_async_16(kv_smem + 8 * kBlkBytes + off_h[h], src_h[h] + 8 * 128, nbytes_h[h]);
@@ -475,10 +488,10 @@ __global__ void __launch_bounds__(kThreads, 1)   // 19 warps: at most 96 registe
                 gok = gok && worker_wait(s_full, gt & 1, abort_flag, p.status);
                 tc_fence_after();
                 float x[kHG];
-                {
+                {   // the two issuers' partial sums
                     uint32_t v[kHG], u[kHG];
-                    tmem_ld16(tmem_base + lane_addr + TM_S + h0, v);        // dims 0..255
-                    tmem_ld16(tmem_base + lane_addr + TM_S + 64 + h0, u);   // dims 256..575
+                    tmem_ld16(tmem_base + lane_addr + TM_S + h0, v);
+                    tmem_ld16(tmem_base + lane_addr + TM_S + 64 + h0, u);
                     tmem_ld_wait();
 #pragma unroll
                     for (int h = 0; h < kHG; ++h) x[h] = __uint_as_float(v[h]) + __uint_as_float(u[h]);
@@ -566,10 +579,9 @@ __global__ void __launch_bounds__(kThreads, 1)   // 19 warps: at most 96 registe
                 }
                 fence_proxy_async_smem();
                 if (any_upd && t > 0) {
-                    // O^T columns of the raised heads: wait for the previous PV (both issuers'
-                    // halves), then rescale in TMEM
-                    gok = gok && worker_wait(&seg_free[1], (gt - 1) & 1, abort_flag, p.status) &&
-                          worker_wait(&seg_free[kSegs - 1], (gt - 1) & 1, abort_flag, p.status);
+                    // O^T columns of the raised heads: wait for the previous PV (every chunk),
+                    // then rescale in TMEM
+                    gok = gok && pv_done(gt - 1);
                     tc_fence_after();
 #pragma unroll 1
                     for (int c = 0; c < 4; ++c) {
@@ -595,8 +607,7 @@ __global__ void __launch_bounds__(kThreads, 1)   // 19 warps: at most 96 registe
                 if ((lane & 1u) == 0) red[quad * kH + h0 + (int)(lane >> 1)] = r;
             }
             if (!named_bar_and(2, kWorkers,
-                               gok && (T == 0 || (worker_wait(&seg_free[1], (gt - 1) & 1, abort_flag, p.status) &&
-                                                  worker_wait(&seg_free[kSegs - 1], (gt - 1) & 1, abort_flag, p.status))))) {
+                               gok && (T == 0 || pv_done(gt - 1)))) {
                 failed = true;
                 break;
             }
