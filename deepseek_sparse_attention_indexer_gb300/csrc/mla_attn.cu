@@ -74,10 +74,9 @@ constexpr int kQBlkBytes = kH * 128;   // 8 KB: 64 heads x 64 dims
 constexpr int kWorkerWarps = 16;                  // gather + softmax warps
 constexpr int kWorkers = kWorkerWarps * 32;        // 512
 constexpr int kIssuers = 2;                        // MMA-issuing warps
-// issuer that owns latent chunk c (its QK segment and its PV); the rope block goes with chunk 3.
-// Interleaved, so that PV frees chunks 0 and 1 first, together, and the next tile's copies of
-// them (issued in chunk order) start as early as they can.
-__host__ __device__ constexpr int chunk_owner(int c) { return c % kIssuers; }
+// Issuer i owns latent chunks i and i + 2 (their QK segments and their PV): interleaved, so that
+// PV frees chunks 0 and 1 first, together, and the next tile's copies of them (issued in chunk
+// order) start as early as they can.  Issuer 1 also runs the QK over the rope block.
 constexpr int kMaxRegs = 96;                       // 19 warps: 5 share one 16K-register sub-partition
 constexpr int kThreads = 32 * (1 + kIssuers) + kWorkers;  // warp 0 Q loader, warps 1-2 MMA, warps 3.. workers
 constexpr int kHG = kH / (kWorkerWarps / 4);       // 16 heads per worker warp
@@ -274,7 +273,9 @@ __global__ void __maxnreg__(kMaxRegs)   // kThreads threads, one CTA per SM
         // two independent issuers reach one per ~48 (four are no faster).  The work splits by
         // 128-dim latent chunk: issuer 0 owns chunks 0 and 2, issuer 1 chunks 1 and 3 and the
         // rope block.  The owner of a chunk runs the QK over its dims into its own S^T partial
-        // sum and the PV for that O^T chunk; the softmax adds the two partial sums.
+        // sum and the PV for that O^T chunk; the softmax adds the two partial sums.  The issuing
+        // thread's instructions per MMA count: each descriptor is a precomputed base plus a
+        // compile-time offset.
         const int iss = warp - 1;
         const uint32_t tm_s = tmem_base + TM_S + 64 * (uint32_t)iss;
         int gt = 0, qi = 0;
@@ -287,30 +288,39 @@ __global__ void __maxnreg__(kMaxRegs)   // kThreads threads, one CTA per SM
             const int T = item_tiles(p, I, lane);
             if (lane == 0) {
                 ok = mbar_wait_spin(q_full, qi & 1, abort_flag, p.status);
-                const uint32_t q_base = smem_u32(sQ);
                 const uint32_t kv_base = smem_u32(sKV);
+                // operand descriptors at the buffers' starts; an MMA's descriptor is one of these
+                // plus its operand's offset in 16-byte units (addresses stay below 256 KB, so the
+                // 14-bit address field never carries)
+                const uint64_t qk_a = sdesc_sw128(kv_base, 16, 1024);
+                const uint64_t qk_b = sdesc_sw128(smem_u32(sQ), 16, 1024);
+                // PV: A = V^T MN-major, 64-dim atoms 16 KB apart (LBO), 8-key groups 1 KB apart
+                // (SBO); B = P^T MN-major, one 64-head atom, 8-key groups 1 KB apart
+                const uint64_t pv_a = sdesc_sw128(kv_base, kBlkBytes, 1024);
+                const uint64_t pv_b = sdesc_sw128(kv_base + 8 * kBlkBytes, kBlkBytes, 1024);
                 bool q_released = false;
                 for (int t = 0; ok && t < T; ++t, ++gt) {
                     // ---- this issuer's part of S^T = K . Q^T, segment by segment as the copies
-                    // land.  Its accumulator needs no wait of its own: the previous tile's
-                    // probabilities (p_full, awaited before its PV) were written after every
-                    // worker had read both partial sums.
-                    bool first = true;
-                    for (int c = 0; c < 5 && ok; ++c) {
-                        if (chunk_owner(c < 4 ? c : 3) != iss) continue;
+                    // land: latent chunks iss and iss + 2, and for issuer 1 the rope block
+                    // (segment 4).  Segment c's K blocks are 2c and 2c + 1 (the rope block is block
+                    // 8), so its descriptors are the bases plus 2c blocks.  The accumulator needs
+                    // no wait of its own: the previous tile's probabilities (p_full, awaited before
+                    // its PV) were written after every worker had read both partial sums.
+#pragma unroll
+                    for (int j = 0; j < 3; ++j) {
+                        if (j == 2 && iss == 0) break;
+                        const int c = (j < 2) ? iss + 2 * j : 4;
                         if (!(ok = mbar_wait_spin(&seg_full[c], gt & 1, abort_flag, p.status))) break;
                         tc_fence_after();
-                        const int b_lo = (c < 4) ? 2 * c : 8;
-                        const int nb = (c < 4) ? 2 : 1;
-                        for (int bb = 0; bb < nb; ++bb) {
-                            const int blk = b_lo + bb;
+                        const uint64_t a_c = qk_a + (uint64_t)(2 * c * (kBlkBytes >> 4));
+                        const uint64_t b_c = qk_b + (uint64_t)(2 * c * (kQBlkBytes >> 4));
 #pragma unroll
-                            for (int kk = 0; kk < 4; ++kk) {
-                                const uint64_t ad = sdesc_sw128(kv_base + blk * kBlkBytes + kk * 32, 16, 1024);
-                                const uint64_t bd = sdesc_sw128(q_base + blk * kQBlkBytes + kk * 32, 16, 1024);
-                                mma_bf16_ss(tm_s, ad, bd, IDESC_QK, first ? 0u : 1u);
-                                first = false;
-                            }
+                        for (int bb = 0; bb < (j < 2 ? 2 : 1); ++bb) {
+#pragma unroll
+                            for (int kk = 0; kk < 4; ++kk)
+                                mma_bf16_ss(tm_s, a_c + (uint64_t)(bb * (kBlkBytes >> 4) + 2 * kk),
+                                            b_c + (uint64_t)(bb * (kQBlkBytes >> 4) + 2 * kk), IDESC_QK,
+                                            (j | bb | kk) ? 1u : 0u);
                         }
                     }
                     if (!ok) break;
@@ -324,18 +334,15 @@ __global__ void __maxnreg__(kMaxRegs)   // kThreads threads, one CTA per SM
                     // copies of that chunk (and then its QK) overlap the rest of this PV
                     if (!(ok = mbar_wait_spin(p_full, gt & 1, abort_flag, p.status))) break;
                     tc_fence_after();
-                    const uint32_t p_base = kv_base + 8 * kBlkBytes;
 #pragma unroll
-                    for (int c = 0; c < 4; ++c) {
-                        if (chunk_owner(c) != iss) continue;
+                    for (int j = 0; j < 2; ++j) {
+                        const int c = iss + 2 * j;
+                        const uint64_t a_c = pv_a + (uint64_t)(2 * c * (kBlkBytes >> 4));
+                        const uint32_t d = tmem_base + TM_O + 64 * (uint32_t)c;
 #pragma unroll
-                        for (int kk = 0; kk < 8; ++kk) {   // 16 keys per K step
-                            // A = V^T: MN-major, 64-dim atoms 16 KB apart (LBO), 8-key groups 1 KB apart (SBO)
-                            const uint64_t ad = sdesc_sw128(kv_base + (2 * c) * kBlkBytes + kk * 2048, kBlkBytes, 1024);
-                            // B = P^T: MN-major, one 64-head atom, 8-key groups 1 KB apart
-                            const uint64_t bd = sdesc_sw128(p_base + kk * 2048, kBlkBytes, 1024);
-                            mma_bf16_ss(tmem_base + TM_O + 64 * c, ad, bd, IDESC_PV, (t > 0 || kk > 0) ? 1u : 0u);
-                        }
+                        for (int kk = 0; kk < 8; ++kk)   // 16 keys (two 8-key groups, 2 KB) per K step
+                            mma_bf16_ss(d, a_c + (uint64_t)(kk * (2048 >> 4)), pv_b + (uint64_t)(kk * (2048 >> 4)),
+                                        IDESC_PV, (t > 0 || kk > 0) ? 1u : 0u);
                         // the copies of the rope block (which P^T overwrites) come after every
                         // chunk's free, so after every issuer's reads of P^T
                         mma_commit(&seg_free[c]);
