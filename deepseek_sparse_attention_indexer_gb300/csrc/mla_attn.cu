@@ -206,6 +206,20 @@ __device__ __forceinline__ float warp_transpose_reduce16(const float (&x)[16], u
     return MAX ? fmaxf(a[0], o) : a[0] + o;
 }
 
+// descriptor halves: the low word (address and LBO fields) plus a 16-byte offset cannot carry into
+// the high word (shared addresses < 256 KB), so only the low word is added to
+__device__ __forceinline__ void mma_bf16_ss_lo(uint32_t d_tmem, uint32_t a_lo, uint32_t a_hi, uint32_t b_lo,
+                                               uint32_t b_hi, uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t.reg .b64 da, db;\n\t"
+        "setp.ne.b32 p, %6, 0;\n\t"
+        "mov.b64 da, {%1, %2};\n\t"
+        "mov.b64 db, {%3, %4};\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %5, p;\n\t}\n" ::"r"(d_tmem),
+        "r"(a_lo), "r"(a_hi), "r"(b_lo), "r"(b_hi), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
 template <bool PARTIAL, bool PAGED>
 __global__ void __maxnreg__(kMaxRegs)   // kThreads threads, one CTA per SM
     mla_sparse_attn_kernel(const __grid_constant__ CUtensorMap tmap_q, const AttnParams p) {
@@ -318,9 +332,10 @@ __global__ void __maxnreg__(kMaxRegs)   // kThreads threads, one CTA per SM
                         for (int bb = 0; bb < (j < 2 ? 2 : 1); ++bb) {
 #pragma unroll
                             for (int kk = 0; kk < 4; ++kk)
-                                mma_bf16_ss(tm_s, a_c + (uint64_t)(bb * (kBlkBytes >> 4) + 2 * kk),
-                                            b_c + (uint64_t)(bb * (kQBlkBytes >> 4) + 2 * kk), IDESC_QK,
-                                            (j | bb | kk) ? 1u : 0u);
+                                mma_bf16_ss_lo(tm_s, (uint32_t)a_c + (uint32_t)(bb * (kBlkBytes >> 4) + 2 * kk),
+                                               (uint32_t)(qk_a >> 32),
+                                               (uint32_t)b_c + (uint32_t)(bb * (kQBlkBytes >> 4) + 2 * kk),
+                                               (uint32_t)(qk_b >> 32), IDESC_QK, (j | bb | kk) ? 1u : 0u);
                         }
                     }
                     if (!ok) break;
@@ -341,8 +356,9 @@ __global__ void __maxnreg__(kMaxRegs)   // kThreads threads, one CTA per SM
                         const uint32_t d = tmem_base + TM_O + 64 * (uint32_t)c;
 #pragma unroll
                         for (int kk = 0; kk < 8; ++kk)   // 16 keys (two 8-key groups, 2 KB) per K step
-                            mma_bf16_ss(d, a_c + (uint64_t)(kk * (2048 >> 4)), pv_b + (uint64_t)(kk * (2048 >> 4)),
-                                        IDESC_PV, (t > 0 || kk > 0) ? 1u : 0u);
+                            mma_bf16_ss_lo(d, (uint32_t)a_c + (uint32_t)(kk * (2048 >> 4)), (uint32_t)(pv_a >> 32),
+                                           (uint32_t)pv_b + (uint32_t)(kk * (2048 >> 4)), (uint32_t)(pv_b >> 32),
+                                           IDESC_PV, (t > 0 || kk > 0) ? 1u : 0u);
                         // the copies of the rope block (which P^T overwrites) come after every
                         // chunk's free, so after every issuer's reads of P^T
                         mma_commit(&seg_free[c]);
