@@ -20,6 +20,7 @@ namespace {
 std::atomic<int32_t*> g_status_ptr[64];
 constexpr int kMaxDevices = 64;
 std::atomic<int> g_sm_count[kMaxDevices];
+std::atomic<int> g_l2_bytes[kMaxDevices];
 std::atomic<int> g_cc_ok[kMaxDevices];  // 0 unknown, 1 ok, 2 not sm_103
 std::mutex g_attr_mu;
 
@@ -66,6 +67,17 @@ int device_sm_count() {
         g_sm_count[dev].store(v);
     }
     return v;
+}
+
+size_t device_l2_bytes() {
+    int dev = current_device();
+    if (dev < 0 || dev >= kMaxDevices) return 0;
+    int v = g_l2_bytes[dev].load();
+    if (v <= 0) {
+        if (cudaDeviceGetAttribute(&v, cudaDevAttrL2CacheSize, dev) != cudaSuccess || v <= 0) v = 0;
+        g_l2_bytes[dev].store(v);
+    }
+    return (size_t)v;
 }
 
 dsa_status_t check_device() {

@@ -11,6 +11,7 @@ namespace dsa {
 
 // Number of SMs of the current device (cached per device).
 int device_sm_count();
+size_t device_l2_bytes();   // L2 size of the current device (0 if unknown)
 // DSA_OK when the current device is compute capability 10.3.
 dsa_status_t check_device();
 // Device address of the sticky error word on the current device (nullptr if

@@ -148,6 +148,11 @@ __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wa
 __device__ __forceinline__ void cp_async_16(uint32_t dst, const void* src, uint32_t src_bytes) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
 }
+// Bring [src, src + bytes) into L2 (bytes a multiple of 16, src 16-byte aligned); no completion
+// to wait for
+__device__ __forceinline__ void l2_prefetch_bulk(const void* src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
 // Arrive on the mbarrier once all of this thread's earlier cp.async are done
 // (no pending-count increment: the barrier's expected count includes it).
 __device__ __forceinline__ void cp_async_arrive_noinc(uint64_t* bar) {

@@ -125,6 +125,7 @@ struct AttnParams {
     float scale_log2;          // scale * log2(e)
     int32_t* status;           // device error word
     PageTable pages;           // paged cache (pages.table == nullptr: dense rows)
+    int l2_prefetch;           // 1: prefetch each tile's cache rows into L2 one tile ahead (dense prefill)
 };
 
 // Waits of the worker warps (every lane polls).
@@ -396,6 +397,11 @@ __global__ void __maxnreg__(kMaxRegs)   // kThreads threads, one CTA per SM
         Item gI{};
         bool g_valid = false;
         int g_j = -1;  // lanes 0..7: key of row 64 (lane / 4) + 4 ww + lane % 4 of the cursor's tile
+        // lanes 0..7: the key at the same row of the tile after the cursor's, with its batch and
+        // bound; the next gather_issue prefetches that cache row into L2, one tile period before
+        // its copy (a cache larger than what L2 keeps would otherwise put HBM latency on every
+        // tile's critical path)
+        int g_jn = -1, g_nbatch = 0, g_nbound = 0;
         auto g_advance_item = [&]() {
             g_valid = false;
             for (;;) {
@@ -416,15 +422,36 @@ __global__ void __maxnreg__(kMaxRegs)   // kThreads threads, one CTA per SM
         // behind the softmax that precedes the copies.
         auto gather_prep = [&]() {
             g_j = -1;
+            g_jn = -1;
             if (g_valid && lane < 8) {
-                const int slot = gI.slot0 + g_t * kTile + 64 * (int)(lane >> 2) + 4 * ww + (int)(lane & 3);
+                const int rowpos = 64 * (int)(lane >> 2) + 4 * ww + (int)(lane & 3);
+                const int slot = gI.slot0 + g_t * kTile + rowpos;
                 g_j = (slot < gI.slot_end) ? __ldg(p.idx + (int64_t)gI.row * p.top_k + slot) : -1;
+                if (!PAGED && !PARTIAL && p.l2_prefetch) {
+                    if (g_t + 1 < g_T) {
+                        const int s2 = slot + kTile;
+                        g_jn = (s2 < gI.slot_end) ? __ldg(p.idx + (int64_t)gI.row * p.top_k + s2) : -1;
+                        g_nbatch = gI.batch;
+                        g_nbound = gI.bound;
+                    } else {
+                        const int it = nth_item(p, g_s);   // the next item's first tile
+                        if (it >= 0) {
+                            const Item J = decode_item(p, it);
+                            const int s2 = J.slot0 + rowpos;
+                            g_jn = (s2 < J.slot_end) ? __ldg(p.idx + (int64_t)J.row * p.top_k + s2) : -1;
+                            g_nbatch = J.batch;
+                            g_nbound = J.bound;
+                        }
+                    }
+                }
             }
         };
         // Issue this warp's copies of the cursor's tile, half by half as PV frees
         // them, then advance the cursor.  Returns false if a wait gave up.
         auto gather_issue = [&]() -> bool {
             if (!g_valid) return true;
+            if (!PAGED && !PARTIAL && g_jn >= 0 && g_jn < g_nbound)   // g_jn stays -1 without l2_prefetch
+                l2_prefetch_bulk(kv_bytes + ((int64_t)g_nbatch * p.Nmax + g_jn) * kRowBytes, kRowBytes);
             int j = g_j;
             if (j >= gI.bound) {
                 raise_dev_error(p.status, DEV_ERR_BOUNDS);
@@ -777,6 +804,11 @@ dsa_status_t launch_attn_prefill(const void* q, const void* kv, const int32_t* i
     p.scale_log2 = scale * 1.4426950408889634f;
     p.status = device_status_ptr();
     p.pages = pages;   // a paged cache: batch 0's table row
+    // The gather reads each tile's rows at random from the cache; once the cache is large against
+    // L2 (measured: a 75 MB cache at a 59% L2 hit rate, a 19 MB one at 94%), each tile's copies
+    // wait for HBM unless their rows were prefetched.  For an L2-resident cache the prefetches
+    // only cost issue slots (1.8% at 19 MB), so they are enabled above a quarter of L2.
+    p.l2_prefetch = (size_t)N * kRowBytes > device_l2_bytes() / 4 ? 1 : 0;
     return p.pages.table ? launch_kernel<false, true>(q, L, p, stream) : launch_kernel<false, false>(q, L, p, stream);
 }
 
