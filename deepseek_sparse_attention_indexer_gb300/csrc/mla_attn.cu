@@ -97,7 +97,8 @@ constexpr int OFF_BAR = OFF_INVL + kH * 4;
 constexpr int N_BARS = 2 + 5 + kSegs + 2;
 constexpr int OFF_TMEM = OFF_BAR + N_BARS * 8;
 constexpr int OFF_ABORT = OFF_TMEM + 4;
-constexpr int SMEM_BYTES = OFF_ABORT + 4 + 1024;
+constexpr int OFF_ITEM_T = OFF_ABORT + 4;              // int: the current item's tile count (workers)
+constexpr int SMEM_BYTES = OFF_ITEM_T + 4 + 1024;
 
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t TM_S = 0;                       // S^T partial sums: issuer i's 64 columns at 64 i
@@ -157,17 +158,31 @@ __device__ __forceinline__ int nth_item(const AttnParams& p, int s) {
 }
 
 // Number of 128-slot tiles up to the last non-negative index of the item's
-// slot range (warp-collective; every lane gets the same answer).
+// slot range (warp-collective; every lane gets the same answer).  A full
+// selection ends with a valid index, so the last 32 slots are looked at first;
+// otherwise (a query with fewer causal keys than top_k: a valid prefix, then
+// -1) the range is scanned backwards 512 slots a round, 16 independent loads a
+// lane, so that a short item costs a few L2 round trips rather than one per 32
+// slots.
 __device__ __forceinline__ int item_tiles(const AttnParams& p, const Item& I, uint32_t lane) {
     const int32_t* ir = p.idx + (int64_t)I.row * p.top_k;
-    for (int base = I.slot_end - 32; base > I.slot0 - 32; base -= 32) {
-        const int s = base + (int)lane;
+    int hi = I.slot_end - 32;   // slots [hi, slot_end) first
+    {
+        const int s = hi + (int)lane;
         const bool v = (s >= I.slot0) && (s < I.slot_end) && (__ldg(ir + s) >= 0);
         const uint32_t m = __ballot_sync(0xffffffffu, v);
-        if (m) {
-            const int last = base + 31 - __clz(m);
-            return (last - I.slot0) / kTile + 1;
+        if (m) return (hi + 31 - __clz(m) - I.slot0) / kTile + 1;
+    }
+    for (; hi > I.slot0; hi -= 512) {   // slots [max(slot0, hi - 512), hi)
+        const int lo = hi - 512;
+        int last = -1;
+#pragma unroll
+        for (int k = 0; k < 16; ++k) {
+            const int s = lo + 32 * k + (int)lane;
+            if (s >= I.slot0 && s < hi && __ldg(ir + s) >= 0) last = s;
         }
+        last = __reduce_max_sync(0xffffffffu, last);
+        if (last >= 0) return (last - I.slot0) / kTile + 1;
     }
     return 0;
 }
@@ -241,6 +256,7 @@ __global__ void __maxnreg__(kMaxRegs)   // kThreads threads, one CTA per SM
     uint64_t* p_full = s_full + 1;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + OFF_TMEM);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + OFF_ABORT);
+    int* item_T = reinterpret_cast<int*>(smem + OFF_ITEM_T);
 
     const int warp = threadIdx.x / 32;
     const uint32_t lane = lane_id();
@@ -524,14 +540,18 @@ __global__ void __maxnreg__(kMaxRegs)   // kThreads threads, one CTA per SM
             if (item == -1) break;
             if (item < 0) continue;
             const Item I = decode_item(p, item);
-            const int T = item_tiles(p, I, lane);
             const int32_t* ir = p.idx + (int64_t)I.row * p.top_k;
-            named_bar_sync(1, kWorkers);  // previous item's readers of m_used / invl are done
+            named_bar_sync(1, kWorkers);  // previous item's readers of m_used / invl / item_T are done
             if (tid < kH) m_used[tid] = -INFINITY;
+            if (ww == 0) {   // one warp finds the item's tile count for all
+                const int tt = item_tiles(p, I, lane);
+                if (lane == 0) *item_T = tt;
+            }
             float l_part[kHG];
 #pragma unroll
             for (int h = 0; h < kHG; ++h) l_part[h] = 0.f;
             named_bar_sync(1, kWorkers);
+            const int T = *item_T;
             for (int t = 0; t < T; ++t, ++gt) {
                 const int slot = I.slot0 + t * kTile + key;
                 const int j = (slot < I.slot_end) ? __ldg(ir + slot) : -1;  // issued before the wait
