@@ -20,6 +20,7 @@ chunk on its own GPU (independent problems, no data-path collective), so
 the host cores, on a bounded sample of the same workload.
 """
 import argparse
+import dataclasses
 import json
 import os
 import statistics
@@ -619,12 +620,20 @@ def main():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(W.WORKLOADS))
     ap.add_argument("--queries", type=int, default=0,
                     help="profiling aid: keep the context, time only the last N queries of the chunk")
+    ap.add_argument("--batch", type=int, default=0,
+                    help="decode workloads: the same step for this many sequences (batch scaling)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     wl = W.WORKLOADS[args.workload]
     if args.queries and args.queries < wl.L:
         wl = W.custom(f"{wl.name}_last{args.queries}", B=wl.B, L=args.queries, p0=wl.N - args.queries, N=wl.N,
                       top_k=wl.top_k, seed=wl.seed, rope_std=wl.rope_std, dup_frac=wl.dup_frac)
+    if args.batch:
+        if wl.L != 1:
+            ap.error("--batch applies to decode workloads")
+        wl = dataclasses.replace(wl, name=f"{wl.name}_batch{args.batch}", B=args.batch,
+                                 desc=f"{args.batch} sequences, one new query each at position {wl.p0} "
+                                      f"over its own {wl.N}-key cache, top_k {wl.top_k}")
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
