@@ -611,6 +611,24 @@ def run_gpu(args, wl, rank, world, local_rank):
     return 0
 
 
+def resolve_workload(name, queries=0, batch=0):
+    """The named workload, narrowed to its last `queries` queries (prefill) or widened to `batch`
+    sequences (decode)."""
+    wl = W.WORKLOADS[name]
+    if queries and queries < wl.L:
+        wl = W.custom(f"{wl.name}_last{queries}", B=wl.B, L=queries, p0=wl.N - queries, N=wl.N,
+                      top_k=wl.top_k, seed=wl.seed, rope_std=wl.rope_std, dup_frac=wl.dup_frac)
+    if batch:
+        if wl.L != 1:
+            raise ValueError("--batch applies to decode workloads")
+        if batch < 1:
+            raise ValueError("--batch must be positive")
+        wl = dataclasses.replace(wl, name=f"{wl.name}_batch{batch}", B=batch,
+                                 desc=f"{batch} sequences, one new query each at position {wl.p0} "
+                                      f"over its own {wl.N}-key cache, top_k {wl.top_k}")
+    return wl
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -624,16 +642,10 @@ def main():
                     help="decode workloads: the same step for this many sequences (batch scaling)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
-    wl = W.WORKLOADS[args.workload]
-    if args.queries and args.queries < wl.L:
-        wl = W.custom(f"{wl.name}_last{args.queries}", B=wl.B, L=args.queries, p0=wl.N - args.queries, N=wl.N,
-                      top_k=wl.top_k, seed=wl.seed, rope_std=wl.rope_std, dup_frac=wl.dup_frac)
-    if args.batch:
-        if wl.L != 1:
-            ap.error("--batch applies to decode workloads")
-        wl = dataclasses.replace(wl, name=f"{wl.name}_batch{args.batch}", B=args.batch,
-                                 desc=f"{args.batch} sequences, one new query each at position {wl.p0} "
-                                      f"over its own {wl.N}-key cache, top_k {wl.top_k}")
+    try:
+        wl = resolve_workload(args.workload, args.queries, args.batch)
+    except ValueError as exc:
+        ap.error(str(exc))
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))

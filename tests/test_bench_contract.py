@@ -89,3 +89,17 @@ def test_each_workload_line_names_its_own_context():
     assert bench.metric_name(W.WORKLOADS["decode_b8"]).startswith("decode us/step")
     names = {bench.metric_name(w) for w in W.WORKLOADS.values() if w.L > 1}
     assert len(names) == len([w for w in W.WORKLOADS.values() if w.L > 1])
+
+
+def test_resolve_workload_narrows_prefill_and_widens_decode():
+    wl = bench.resolve_workload("prefill_16k", queries=1024)
+    assert (wl.B, wl.L, wl.p0, wl.N, wl.top_k) == (1, 1024, 16384 - 1024, 16384, 2048)
+    wl = bench.resolve_workload("decode_b8", batch=128)
+    assert (wl.B, wl.L, wl.p0, wl.N, wl.top_k) == (128, 1, 4095, 4096, 2048)
+    assert wl.name == "decode_b8_batch128" and "128 sequences" in wl.desc
+    assert bench.metric_name(wl).startswith("decode us/step") and "batch 128" in bench.metric_name(wl)
+    paged = bench.resolve_workload("decode_b8_paged", batch=16)
+    assert paged.page_size == W.WORKLOADS["decode_b8_paged"].page_size and paged.B == 16
+    assert bench.resolve_workload("prefill_16k") == W.WORKLOADS["prefill_16k"]
+    with pytest.raises(ValueError):
+        bench.resolve_workload("prefill_16k", batch=4)
