@@ -48,7 +48,8 @@ constexpr int kHi = DSA_INDEXER_HEADS;  // 32
 constexpr int kDi = DSA_INDEXER_DIM;    // 128
 constexpr int kTileKeys = 128;          // MMA M
 constexpr int kEpiWarps = 16;           // four per TMEM lane quadrant, one query each
-constexpr int kThreads = (2 + kEpiWarps) * 32;   // 576: 18 warps, at most 96 registers a thread
+constexpr int kIssuers = 2;              // MMA-issuing warps, alternating key tiles
+constexpr int kThreads = (1 + kIssuers + kEpiWarps) * 32;   // 19 warps, at most 96 registers a thread
 
 struct IndexerParams {
     const float* w;
@@ -164,7 +165,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&a_empty[s], 1);
         }
         mbar_init(b_full, 1);
-        mbar_init(b_empty, 1);
+        mbar_init(b_empty, kIssuers);   // each issuer's last MMA of an item has read the queries
         for (int a = 0; a < C::NACC; ++a) {
             mbar_init(&acc_full[a], 1);
             mbar_init(&acc_empty[a], kEpiWarps * 32);
@@ -234,11 +235,23 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
         }
-    } else if (warp == 1) {
-        // ------------------------------------------------------------ MMA issuer
+    } else if (warp <= kIssuers) {
+        // ------------------------------------------------------------ MMA issuers
+        // Issuer i takes the key tiles whose running index is i mod kIssuers, so each stage and
+        // each accumulator (both rings of even size) belongs to one issuer, and one issuer's
+        // barrier waits overlap the other's MMAs.  Descriptors are precomputed bases plus
+        // compile-time offsets added to the low word (shared addresses < 256 KB cannot carry).
+        // (Measured: 305 -> 300 us at the 16k chunk; the N = 128 MMAs of this GEMM already ran
+        // close to the tensor rate with one issuer, unlike the attention's N = 64 ones.)
+        static_assert(STAGES % kIssuers == 0 && C::NACC % kIssuers == 0, "rings split evenly over the issuers");
+        const int iss = warp - 1;
         if (lane == 0) {
             int it = 0, bi = 0, acc_it = 0;
             bool ok = true;
+            const uint64_t a_desc = sdesc_sw128(smem_u32(sA), 16, 1024);
+            const uint64_t b_desc = sdesc_sw128(smem_u32(sB), 16, 1024);
+            const uint32_t a_hi = (uint32_t)(a_desc >> 32), b_hi = (uint32_t)(b_desc >> 32);
+            const uint32_t b_lo = (uint32_t)b_desc;
             for (int s = 0; ok; ++s) {
                 int item = nth_item(p, s);
                 if (item == -1) break;
@@ -248,23 +261,22 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (!(ok = mbar_wait_spin(b_full, bi & 1, abort_flag, p.status))) break;
                 ++bi;
                 tc_fence_after();
-                const uint32_t b_base = smem_u32(sB);
                 for (int t = I.t_begin; t < I.n_comp_end; ++t, ++it, ++acc_it) {
+                    if (it % kIssuers != iss) continue;
                     const int st = it % STAGES;
                     const int acc = acc_it % C::NACC;
                     if (!(ok = mbar_wait_spin(&a_full[st], (it / STAGES) & 1, abort_flag, p.status))) break;
                     if (!(ok = mbar_wait_spin(&acc_empty[acc], ((acc_it / C::NACC) & 1) ^ 1, abort_flag, p.status))) break;
                     tc_fence_after();
-                    const uint32_t a_base = smem_u32(sA + st * C::A_BYTES);
+                    const uint32_t a_lo = (uint32_t)a_desc + (uint32_t)(st * (C::A_BYTES >> 4));
                     const uint32_t d = tmem_base + acc * C::N;
 #pragma unroll
                     for (int kb = 0; kb < 2; ++kb) {
 #pragma unroll
-                        for (int kk = 0; kk < 4; ++kk) {
-                            uint64_t ad = sdesc_sw128(a_base + kb * C::A_HALF + kk * 32, 16, 1024);
-                            uint64_t bd = sdesc_sw128(b_base + kb * C::B_HALF + kk * 32, 16, 1024);
-                            mma_bf16_ss(d, ad, bd, C::IDESC, (kb | kk) != 0);
-                        }
+                        for (int kk = 0; kk < 4; ++kk)
+                            mma_bf16_ss_lo(d, a_lo + (uint32_t)(kb * (C::A_HALF >> 4) + 2 * kk), a_hi,
+                                           b_lo + (uint32_t)(kb * (C::B_HALF >> 4) + 2 * kk), b_hi, C::IDESC,
+                                           (kb | kk) != 0);
                     }
                     mma_commit(&a_empty[st]);
                     mma_commit(&acc_full[acc]);
@@ -273,11 +285,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         }
     } else {
-        // ------------------------------------------------------------ epilogue (warps 2..17)
+        // ------------------------------------------------------------ epilogue (warps 1 + kIssuers ..)
         // kEpiWarps / 4 warps per TMEM lane quadrant, one of the group's queries
         // each (warps whose query is past the group's end only write -inf).
         static_assert(QG <= kEpiWarps / 4, "one query per epilogue warp");
-        const int e = warp - 2;                      // 0..kEpiWarps-1
+        const int e = warp - 1 - kIssuers;           // 0..kEpiWarps-1
         const int quad = warp & 3;                   // TMEM lane quadrant of this warp
         const int q = e >> 2;                        // this warp's query within the group
         const int key_in_tile = quad * 32 + (int)lane;

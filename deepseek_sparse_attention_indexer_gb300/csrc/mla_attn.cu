@@ -222,19 +222,6 @@ __device__ __forceinline__ float warp_transpose_reduce16(const float (&x)[16], u
     return MAX ? fmaxf(a[0], o) : a[0] + o;
 }
 
-// descriptor halves: the low word (address and LBO fields) plus a 16-byte offset cannot carry into
-// the high word (shared addresses < 256 KB), so only the low word is added to
-__device__ __forceinline__ void mma_bf16_ss_lo(uint32_t d_tmem, uint32_t a_lo, uint32_t a_hi, uint32_t b_lo,
-                                               uint32_t b_hi, uint32_t idesc, uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t.reg .b64 da, db;\n\t"
-        "setp.ne.b32 p, %6, 0;\n\t"
-        "mov.b64 da, {%1, %2};\n\t"
-        "mov.b64 db, {%3, %4};\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %5, p;\n\t}\n" ::"r"(d_tmem),
-        "r"(a_lo), "r"(a_hi), "r"(b_lo), "r"(b_hi), "r"(idesc), "r"(accumulate)
-        : "memory");
-}
 
 template <bool PARTIAL, bool PAGED>
 __global__ void __maxnreg__(kMaxRegs)   // kThreads threads, one CTA per SM
