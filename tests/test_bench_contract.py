@@ -103,3 +103,16 @@ def test_resolve_workload_narrows_prefill_and_widens_decode():
     assert bench.resolve_workload("prefill_16k") == W.WORKLOADS["prefill_16k"]
     with pytest.raises(ValueError):
         bench.resolve_workload("prefill_16k", batch=4)
+
+
+def test_cpu_baseline_sizes_its_sample_from_a_probe():
+    """The CPU baseline (the oracle on the host's cores) times a seeded sample sized from a short
+    probe to about the target seconds, and says what it timed."""
+    wl = W.custom("cpu_base_small", B=1, L=48, p0=464, N=512, top_k=128, seed=3)
+    inputs = bench.make_inputs(wl)
+    cb = bench.cpu_baseline(wl, inputs, decode=False, target_s=0.05)
+    assert cb["kind"] == "oracle" and cb["unit"] == bench.UNIT and cb["value"] > 0 and cb["cores"] >= 1
+    assert "query rows" in cb["sample"]
+    wl_d = W.custom("cpu_base_decode", B=2, L=1, p0=255, N=256, top_k=64, seed=4)
+    cb = bench.cpu_baseline(wl_d, bench.make_inputs(wl_d), decode=True, target_s=0.05)
+    assert cb["unit"] == "us/step" and cb["value"] > 0 and "decode steps" in cb["sample"]
