@@ -70,6 +70,15 @@ def algorithmic(wl):
     }
 
 
+def step_roofline(work, peak_tflops, hbm_gbs, step_ms):
+    """The step's ideal time (indexer FLOP at the bf16 peak + causal score bytes at the HBM rate +
+    attention FLOP at the bf16 peak) and the measured step's fraction of it."""
+    ideal_ms = 1e3 * (work["indexer_flop"] / (peak_tflops * 1e12) + work["topk_bytes"] / (hbm_gbs * 1e9)
+                      + work["attn_flop"] / (peak_tflops * 1e12))
+    return {"ideal_ms": ideal_ms, "measured_ms": float(step_ms), "frac": ideal_ms / float(step_ms),
+            "terms": "indexer FLOP / bf16 peak + causal score bytes / HBM + attention FLOP / bf16 peak"}
+
+
 def max_over_ranks(x, world, device=None):
     """The slowest rank's value (the job ends when its last rank does).  One rank: x itself.  The
     collective runs on the process group's backend (NCCL on the GPU machine, gloo in the CPU tests)."""
@@ -574,6 +583,8 @@ def run_gpu(args, wl, rank, world, local_rank):
         "roofline": roof,
         # indexer + top-k per chunk (the selection stage on its own)
         "indexer_topk_ms": float(kern_ms[0] + kern_ms[1]),
+        # the step against its ideal: every kernel at its own roofline, back to back
+        "step_roofline": step_roofline(work, peak, hbm, step_ms_max),
         "kernels_ms": {"dsa_indexer_scores": float(kern_ms[0]), "dsa_topk": float(kern_ms[1]),
                        attn_name: float(kern_ms[2])},
         "kernel_rooflines": {

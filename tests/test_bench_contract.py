@@ -116,3 +116,11 @@ def test_cpu_baseline_sizes_its_sample_from_a_probe():
     wl_d = W.custom("cpu_base_decode", B=2, L=1, p0=255, N=256, top_k=64, seed=4)
     cb = bench.cpu_baseline(wl_d, bench.make_inputs(wl_d), decode=True, target_s=0.05)
     assert cb["unit"] == "us/step" and cb["value"] > 0 and "decode steps" in cb["sample"]
+
+
+def test_step_roofline_of_the_16k_chunk():
+    """The step's ideal: indexer FLOP / peak + score bytes / HBM + attention FLOP / peak."""
+    work = bench.algorithmic(W.WORKLOADS["prefill_16k"])
+    r = bench.step_roofline(work, 1899.5, 6783.5, 1.8)
+    want = 1e3 * (481.1e9 / 1899.5e12 + 234.9e6 / 6783.5e9 + 1168.2e9 / 1899.5e12)
+    assert abs(r["ideal_ms"] - want) < 2e-3 and abs(r["frac"] - want / 1.8) < 2e-3
