@@ -443,6 +443,18 @@ def test_decode_many_sequences(dsa, oracle_mod):
     run_decode_chain(dsa, oracle_mod, wl, kv_len)
 
 
+@pytest.mark.parametrize("B,N", [(64, 4096), (128, 2304)])
+def test_decode_long_items_with_l2_prefetch(dsa, oracle_mod, B, N):
+    """Batches large enough that each split is 8 (B = 64) or 16 (B = 128) tiles, over caches
+    (302 / 340 MB) larger than a quarter of L2: the path that prefetches each item's next tile into
+    L2.  Ragged lengths (a short cache, exactly top_k, top_k + 1) ride along."""
+    wl = W.custom(f"decode_prefetch_b{B}", B=B, L=1, p0=0, N=N, top_k=2048, seed=47 + B)
+    rng = np.random.default_rng(48 + B)
+    kv_len = rng.integers(2049, wl.N + 1, size=wl.B)
+    kv_len[:3] = [100, 2048, 2049]
+    run_decode_chain(dsa, oracle_mod, wl, kv_len)
+
+
 # ----------------------------------------------------------------------------- paged caches
 
 def run_paged_decode_chain(dsa, oracle_mod, wl, kv_len, page_size, corrupt=None):
