@@ -614,6 +614,24 @@ def test_host_prefill_two_sets_overlaps_consecutive_chunks(dsa):
     assert dsa.device_status() == 0
 
 
+@pytest.mark.parametrize("top_k", [1, 200])
+def test_chain_l2_prefetch_short_items(dsa, oracle_mod, top_k):
+    """A 40000-key cache (46 MB, above a quarter of L2, so each tile's rows are prefetched one tile
+    ahead) with one- and two-tile queries: the prefetch runs across query boundaries all the time.
+    Every output row is checked."""
+    wl = W.custom(f"prefetch_short_k{top_k}", B=1, L=160, p0=39840, N=40000, top_k=top_k, seed=67 + top_k)
+    (qi, ki, w, q, kv, q_pos0, kv_len), S, idx, out, lse = run_chain(dsa, wl)
+    th = oracle_mod.default_threads()
+    S_ref = oracle_mod.indexer(qi, ki, w, q_pos0, kv_len, threads=th)
+    np.testing.assert_array_equal(S[0, :, : wl.N].cpu().numpy().astype(np.float64), S_ref)
+    idx_ref = oracle_mod.topk(S_ref.astype(np.float32), q_pos0, kv_len, 1, wl.L, wl.top_k, threads=th)
+    np.testing.assert_array_equal(idx[0].cpu().numpy(), idx_ref)
+    o_ref, l_ref = oracle_mod.attention(q[0], kv, idx_ref, np.zeros(wl.L, np.int32), W.SCALE, threads=th)
+    attn_close(out.float().cpu().numpy(), o_ref, wl.name)
+    np.testing.assert_allclose(lse.cpu().numpy(), l_ref, rtol=1e-5, atol=1e-5)
+    assert dsa.device_status() == 0
+
+
 def test_chain_128k_keys(dsa, oracle_mod):
     """Beyond the configs: 16 queries at the end of a 131072-key context (the streaming top-k, 1024
     key tiles per indexer query group), every output checked."""
