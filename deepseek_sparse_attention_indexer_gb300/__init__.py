@@ -17,7 +17,8 @@ decode step -- uploads, the library calls and the download -- as one CUDA graph
 _API = ("indexer_scores", "topk", "mla_sparse_attn_prefill", "mla_sparse_attn_decode",
         "mla_sparse_attn_decode_noalloc", "indexer_scores_paged", "mla_sparse_attn_decode_paged",
         "mla_sparse_attn_prefill_paged", "mla_value_up_proj", "indexer_source_layer",
-        "attn_workspace_size", "device_status", "status_string", "load", "lib_path", "DsaError")
+        "attn_workspace_size", "device_status", "selftest_wait_timeout", "status_string", "load", "lib_path",
+        "DsaError")
 
 __all__ = list(_API) + ["workloads", "build", "HostPrefill", "HostDecode", "sharding"]
 

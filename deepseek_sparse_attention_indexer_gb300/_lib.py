@@ -50,6 +50,7 @@ SIGNATURES = {
     "mla_value_up_proj": (ctypes.c_int32, [_P, _P, _I, _P, _P]),
     "dsa_indexer_source_layer": (ctypes.c_int, [_I, _I, _I]),
     "dsa_device_status": (ctypes.c_int32, [_P, ctypes.POINTER(ctypes.c_int32), _I]),
+    "dsa_selftest_wait_timeout": (ctypes.c_int32, [_I, ctypes.c_uint64, _P]),
 }
 
 _lock = threading.Lock()
@@ -313,6 +314,14 @@ def indexer_source_layer(layer: int, topk_freq: int = 4, skip_offset: int = 3) -
     if r < 0:
         raise ValueError(f"invalid layer schedule arguments ({layer}, {topk_freq}, {skip_offset})")
     return r
+
+
+def selftest_wait_timeout(spin: bool = False, limit_ns: int = 1_000_000, stream=None) -> None:
+    """Launch the failure-detection self-test: one thread waits, with the kernels' bounded wait
+    (spin: the polling form), on an mbarrier nothing arrives on; the wait gives up after limit_ns
+    and the timeout shows in device_status()."""
+    rc = load().dsa_selftest_wait_timeout(1 if spin else 0, ctypes.c_uint64(int(limit_ns)), _stream(stream))
+    _check("dsa_selftest_wait_timeout", rc)
 
 
 def device_status(reset: bool = True, stream=None) -> int:

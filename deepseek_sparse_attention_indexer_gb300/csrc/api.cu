@@ -129,6 +129,24 @@ dsa_status_t make_tmap_bf16_2d(CUtensorMap* map, const void* base, uint64_t cols
 
 using namespace dsa;
 
+namespace selftest {
+// One thread waits, with the kernels' bounded wait routine, for phase 0 of a fresh mbarrier that
+// nothing arrives on: the wait gives up after limit_ns and records the timeout in the status word.
+__global__ void wait_timeout_selftest_kernel(int32_t* status, uint64_t limit_ns, int spin) {
+    __shared__ __align__(8) uint64_t bar;
+    __shared__ int abort_flag;
+    if (threadIdx.x != 0) return;
+    mbar_init(&bar, 1);
+    abort_flag = 0;
+    fence_mbar_init();
+    volatile int* abort_ptr = &abort_flag;
+    if (spin)
+        (void)mbar_wait_spin(&bar, 0, abort_ptr, status, limit_ns);
+    else
+        (void)mbar_wait(&bar, 0, abort_ptr, status, limit_ns);
+}
+}  // namespace selftest
+
 extern "C" {
 
 const char* dsa_status_string(dsa_status_t s) {
@@ -337,6 +355,15 @@ int dsa_indexer_source_layer(int layer, int topk_freq, int skip_offset) {
     // layers skip_offset + topk_freq - 1, + 2 topk_freq - 1, ... run the indexer
     const int k = (int)(((long long)layer - skip_offset + 1) % topk_freq);
     return layer - k;
+}
+
+dsa_status_t dsa_selftest_wait_timeout(int spin, uint64_t limit_ns, void* stream) {
+    if (spin != 0 && spin != 1) return DSA_ERR_INVALID_ARG;
+    if (limit_ns == 0 || limit_ns > 1000000000ull) return DSA_ERR_INVALID_ARG;
+    dsa_status_t st = check_device();
+    if (st != DSA_OK) return st;
+    selftest::wait_timeout_selftest_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(device_status_ptr(), limit_ns, spin);
+    return cudaGetLastError() == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
 }
 
 dsa_status_t dsa_device_status(void* stream, int32_t* code_out, int reset) {

@@ -34,8 +34,8 @@
 extern "C" {
 #endif
 
-#define DSA_ABI_VERSION 4  /* 2: paged-cache entry points; 3: value up-projection, indexer layer schedule;
-                              4: attention output element type (out_dtype) */
+#define DSA_ABI_VERSION 5  /* 2: paged-cache entry points; 3: value up-projection, indexer layer schedule;
+                              4: attention output element type (out_dtype); 5: wait-timeout self-test */
 
 #define DSA_INDEXER_HEADS 32
 #define DSA_INDEXER_DIM 128
@@ -306,6 +306,22 @@ dsa_status_t mla_value_up_proj(const void *o, const void *wv_b, int R, void *v, 
  * skip_offset < 1).  Host-only, pure function.
  */
 int dsa_indexer_source_layer(int layer, int topk_freq, int skip_offset);
+
+/*
+ * dsa_selftest_wait_timeout -- failure-detection self-test of the kernels'
+ * bounded waits.  Launches one CTA on `stream` whose first thread waits, with
+ * the same wait routine the kernels use (spin = 0: the suspending try_wait
+ * form of the worker warps; spin = 1: the polling test_wait form of the MMA
+ * issuers and loaders), on a fresh mbarrier that nothing arrives on.  The wait
+ * gives up after `limit_ns` nanoseconds of the global timer, records
+ * DSA_ERR_DEVICE_TIMEOUT in the device status word (dsa_device_status reads
+ * it) and the kernel returns; the context stays usable.  Nothing faults,
+ * traps or hangs.
+ * Errors (host, before any launch): DSA_ERR_INVALID_ARG unless spin is 0 or 1
+ * and 0 < limit_ns <= 1e9; DSA_ERR_UNSUPPORTED_DEVICE; DSA_ERR_CUDA when the
+ * launch fails.
+ */
+dsa_status_t dsa_selftest_wait_timeout(int spin, uint64_t limit_ns, void *stream);
 
 /*
  * dsa_device_status -- synchronise `stream`, then read (and if `reset` is

@@ -32,7 +32,8 @@ def test_header_declares_the_path():
     for n in ["dsa_indexer_scores", "dsa_topk", "mla_sparse_attn_prefill", "mla_sparse_attn_decode",
               "dsa_status_string", "dsa_abi_version", "dsa_device_status", "dsa_topk_workspace_size",
               "mla_sparse_attn_workspace_size", "dsa_indexer_scores_paged", "mla_sparse_attn_decode_paged",
-              "mla_sparse_attn_prefill_paged", "mla_value_up_proj", "dsa_indexer_source_layer"]:
+              "mla_sparse_attn_prefill_paged", "mla_value_up_proj", "dsa_indexer_source_layer",
+              "dsa_selftest_wait_timeout"]:
         assert n in names
 
 
@@ -48,7 +49,7 @@ def test_exports_every_declared_symbol(lib):
 
 
 def test_version_and_strings(lib):
-    assert lib.dsa_abi_version() == 4
+    assert lib.dsa_abi_version() == 5
     for code in range(0, 10):
         s = lib.dsa_status_string(code)
         assert s and len(s) > 1
@@ -127,3 +128,14 @@ def test_package_fails_loudly_without_library(tmp_path):
             _lib.load(str(tmp_path / "nope.so"))
     finally:
         _lib._lib = saved
+
+
+def test_wait_timeout_selftest_validates_before_any_launch(lib):
+    """The failure-detection self-test rejects a spin flag other than 0/1 and a limit outside
+    (0, 1 s] on the host (DSA_ERR_INVALID_ARG = 1), before touching the device."""
+    import ctypes
+    f = lib.dsa_selftest_wait_timeout
+    assert f(2, ctypes.c_uint64(1000000), None) == 1
+    assert f(-1, ctypes.c_uint64(1000000), None) == 1
+    assert f(0, ctypes.c_uint64(0), None) == 1
+    assert f(1, ctypes.c_uint64(1000000001), None) == 1

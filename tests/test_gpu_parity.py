@@ -681,3 +681,27 @@ def test_host_decode_graph_replays_match_device_calls(dsa):
         torch.cuda.synchronize()
         assert torch.equal(h_out, ref.cpu()), f"step {step}"
     assert dsa.device_status() == 0
+
+
+# ----------------------------------------------------------------------------- failure detection
+
+@pytest.mark.parametrize("spin", [False, True])
+def test_bounded_wait_reports_timeout_and_the_context_stays_usable(dsa, oracle_mod, spin):
+    """The kernels' bounded wait (both forms), on an mbarrier that nothing arrives on, gives up
+    after its limit and records DSA_ERR_DEVICE_TIMEOUT (6) in the status word; the context then
+    runs the path as before."""
+    import time
+    dsa.device_status()                               # start from a clear word
+    t0 = time.perf_counter()
+    dsa.selftest_wait_timeout(spin=spin, limit_ns=2_000_000)
+    assert dsa.device_status() == 6
+    assert time.perf_counter() - t0 < 10.0
+    assert dsa.device_status() == 0                   # read-and-clear
+    wl = W.custom("after_timeout", B=1, L=8, p0=248, N=256, top_k=64, seed=5)
+    (qi, ki, w, q, kv, q_pos0, kv_len), S, idx, out, lse = run_chain(dsa, wl)
+    S_ref = oracle_mod.indexer(qi, ki, w, q_pos0, kv_len, threads=1)
+    idx_ref = oracle_mod.topk(S_ref.astype(np.float32), q_pos0, kv_len, 1, wl.L, wl.top_k, threads=1)
+    np.testing.assert_array_equal(idx[0].cpu().numpy(), idx_ref)
+    o_ref, _ = oracle_mod.attention(q[0], kv, idx_ref, np.zeros(wl.L, np.int32), W.SCALE, threads=1)
+    attn_close(out.float().cpu().numpy(), o_ref, wl.name)
+    assert dsa.device_status() == 0
