@@ -91,6 +91,7 @@ class HostPrefill:
         return an event that completes when `h_out` holds the result.  The copies and kernels run on
         the runner's own streams; with one set `stream` also waits for that event (the chunk ends
         when its last output slice is on the host), with two it does not."""
+        self._check(h_qi, h_ki, h_w, h_pos, h_len, h_q, h_kv, h_out)
         main = stream if stream is not None else torch.cuda.current_stream(self.dev)
         ds = self.sets[self.calls % len(self.sets)]
         self.calls += 1
@@ -136,6 +137,23 @@ class HostPrefill:
         if len(self.sets) == 1:
             main.wait_event(finished)
         return finished
+
+
+    def _check(self, h_qi, h_ki, h_w, h_pos, h_len, h_q, h_kv, h_out):
+        """Host buffers must match this runner's shapes (16-bit data as bf16 bits in int16 or
+        bfloat16) before anything is enqueued."""
+        ds = self.sets[0]
+        for name, h, d in (("h_qi", h_qi, ds.qi), ("h_ki", h_ki, ds.ki), ("h_w", h_w, ds.w), ("h_pos", h_pos, ds.pos),
+                           ("h_len", h_len, ds.len), ("h_q", h_q, ds.q), ("h_kv", h_kv, ds.kv), ("h_out", h_out, ds.out)):
+            if tuple(h.shape) != tuple(d.shape):
+                raise ValueError(f"{name}: expected shape {tuple(d.shape)}, got {tuple(h.shape)}")
+            # 16-bit data may be bf16 bits in either int16 or bfloat16; 32-bit data must match kind
+            if h.element_size() != d.element_size() or (d.element_size() == 4 and h.dtype != d.dtype):
+                raise ValueError(f"{name}: expected {d.dtype} (or the same bits), got {h.dtype}")
+            if h.is_cuda:
+                raise ValueError(f"{name}: expected a host tensor (pinned for asynchronous copies)")
+            if not h.is_contiguous():
+                raise ValueError(f"{name}: expected a contiguous tensor")
 
 
 def _as(h: torch.Tensor, like: torch.Tensor) -> torch.Tensor:

@@ -632,6 +632,25 @@ def test_chain_l2_prefetch_short_items(dsa, oracle_mod, top_k):
     assert dsa.device_status() == 0
 
 
+def test_host_prefill_rejects_mismatched_host_buffers(dsa):
+    """A host buffer of the wrong shape, dtype width or device raises before anything is enqueued."""
+    from deepseek_sparse_attention_indexer_gb300.host_prefill import HostPrefill
+    L, N, K = 16, 1040, 256
+    runner = HostPrefill(L, N, K, slices=1)
+    good = [torch.zeros((1, L, 32, 128), dtype=torch.int16), torch.zeros((1, N, 128), dtype=torch.int16),
+            torch.zeros((1, L, 32), dtype=torch.float32), torch.zeros((1,), dtype=torch.int32),
+            torch.zeros((1,), dtype=torch.int32), torch.zeros((1, L, 64, 576), dtype=torch.int16),
+            torch.zeros((1, N, 576), dtype=torch.int16), torch.zeros((L, 64, 512), dtype=torch.float32)]
+    for k, bad in ((5, torch.zeros((1, L, 64, 512), dtype=torch.int16)),      # q with 512 dims
+                   (2, torch.zeros((1, L, 32), dtype=torch.float64)),         # weights of the wrong width
+                   (7, torch.zeros((L, 64, 512), dtype=torch.float32, device="cuda"))):   # device output
+        args = list(good)
+        args[k] = bad
+        with pytest.raises(ValueError):
+            runner(*args, W.SCALE)
+    assert runner.calls == 0
+
+
 def test_chain_128k_keys(dsa, oracle_mod):
     """Beyond the configs: 16 queries at the end of a 131072-key context (the streaming top-k, 1024
     key tiles per indexer query group), every output checked."""
