@@ -429,6 +429,7 @@ def run_gpu(args, wl, rank, world, local_rank):
     d2h = host_out.numel() * host_out.element_size()
 
     e2e_pipelined = False
+    e2e_rounds = None
     if not decode and wl.B == 1:
         # the package's host-buffer prefill: copies on side streams overlap the kernels
         from deepseek_sparse_attention_indexer_gb300.host_prefill import HostPrefill
@@ -496,15 +497,19 @@ def run_gpu(args, wl, rank, world, local_rank):
         for k in range(2):
             e2e_step(k)
         torch.cuda.synchronize()
-        e0 = torch.cuda.Event(enable_timing=True)
-        e1 = torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for k in range(n_chunks):
-            done = e2e_step(k)
-        stream.wait_event(done)
-        e1.record(stream)
-        torch.cuda.synchronize()
-        e2e_mean = max_over_ranks(e0.elapsed_time(e1) / n_chunks, world, dev)
+        rounds = []
+        for _ in range(3):        # median of three rounds: host copies share the box's memory system
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for k in range(n_chunks):
+                done = e2e_step(k)
+            stream.wait_event(done)
+            e1.record(stream)
+            torch.cuda.synchronize()
+            rounds.append(e0.elapsed_time(e1) / n_chunks)
+        e2e_rounds = [round(r, 4) for r in rounds]
+        e2e_mean = max_over_ranks(float(np.median(rounds)), world, dev)
     else:
         e2e_mean = max_over_ranks(e2e_single, world, dev)
 
@@ -595,7 +600,8 @@ def run_gpu(args, wl, rank, world, local_rank):
         },
         "e2e": {"value": e2e_value, "unit": unit,
                 "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "api": e2e_api,
-                "ms_per_step": round(e2e_mean, 4), "single_step_latency_ms": round(e2e_single, 4)},
+                "ms_per_step": round(e2e_mean, 4), "single_step_latency_ms": round(e2e_single, 4),
+                **({"rounds_ms_per_step": e2e_rounds} if e2e_rounds else {})},
         "graph": ({"ms_per_step": graph_ms, "note": "the step replayed as one CUDA graph, inputs resident, "
                    "no L2 flush between replays"} if isinstance(graph_ms, float) else {"ms_per_step": None,
                                                                                      "note": graph_ms}),
