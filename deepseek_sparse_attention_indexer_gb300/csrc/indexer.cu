@@ -18,8 +18,9 @@
 //     lane, relu, times the head weight, summed -- no cross-thread traffic and
 //     no per-head [L, N] tensor ever exists.  Each warp then stores 32
 //     consecutive keys of a score row (128-byte coalesced stores).
-//   * Warp roles: warp 0 issues TMA, warp 1 issues the MMAs (one thread), warps
-//     2..17 run the epilogue, four per TMEM lane quadrant, one query each:
+//   * Warp roles: warp 0 issues TMA, warps 1 and 2 issue the MMAs (one thread
+//     each, alternating key tiles), warps 3..18 run the epilogue, four per TMEM
+//     lane quadrant, one query each:
 //     with four epilogue warps per scheduler, one warp's TMEM loads hide
 //     behind the others' arithmetic, and a warp's query keeps its 32 head
 //     weights in registers for the whole item.  (Eight-query groups, N = 256,

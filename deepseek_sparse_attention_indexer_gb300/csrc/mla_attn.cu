@@ -30,10 +30,18 @@
 //     The copies of tile t+1 are issued right after the warp's softmax of
 //     tile t, so the whole CTA issues copies (cp.async throughput from L2
 //     grows with the number of issuing warps).  QK waits per 128-dim chunk of
-//     the K-dim.  Unselected or padding slots are zero-filled.  (Timing
-//     variants without any copies ran as fast: the MMA stream and the softmax
-//     between QK and PV bound a tile, and one 144 KB stage plus the 72 KB
-//     Q^T leave no room for a second tile or query to overlap them.)
+//     the K-dim.  Unselected or padding slots are zero-filled.  Above a
+//     quarter of L2 of cache, each lane also prefetches into L2 the row it
+//     copies one tile later.
+//   * Two MMA-issuing warps: one issuing thread sustains an M128 N64 K16 MMA
+//     only every ~70 cycles, two reach one every ~48 per SM.  Issuer i owns
+//     latent chunks i and i + 2 (their QK into its own S^T partial sum, which
+//     the softmax adds, and their PV); issuer 1 also the rope block.  The
+//     issuing threads are instruction-bound, so each descriptor is a
+//     precomputed base plus a compile-time offset on its low word.  What
+//     bounds a tile is the shared-memory traffic of the operands and copies
+//     plus the softmax between QK and PV: one 144 KB stage and the 72 KB Q^T
+//     leave no room for a second tile or query to overlap it.
 //   * Paged caches (PAGED): a row's cache address comes from the sequence's
 //     page table, looked up after the index load.
 //   * Softmax: four warps per TMEM lane quadrant, 16 heads each, one key per
