@@ -97,8 +97,8 @@ constexpr float kRescaleThreshold = 16.0f;  // log2 units
 constexpr int OFF_Q = 0;                               // 9 x 8 KB
 constexpr int OFF_KV = OFF_Q + 9 * kQBlkBytes;         // 9 x 16 KB (block 8 = rope, then P^T)
 constexpr int OFF_RED = OFF_KV + 9 * kBlkBytes;        // float [4][64]
-constexpr int OFF_MUSED = OFF_RED + 4 * kH * 4;        // float [64]
-constexpr int OFF_ALPHA = OFF_MUSED + kH * 4;          // float [64]
+constexpr int OFF_MNEG = OFF_RED + 4 * kH * 4;         // float [64]: minus the reference maxima
+constexpr int OFF_ALPHA = OFF_MNEG + kH * 4;          // float [64]
 constexpr int OFF_INVL = OFF_ALPHA + kH * 4;           // float [64]
 constexpr int OFF_BAR = OFF_INVL + kH * 4;
 // barriers: q_full, q_empty, seg_full[5], seg_free[4], s_full, p_full
@@ -239,7 +239,7 @@ __global__ void __maxnreg__(kMaxRegs)   // kThreads threads, one CTA per SM
     uint8_t* sQ = smem + OFF_Q;
     uint8_t* sKV = smem + OFF_KV;
     float* red = reinterpret_cast<float*>(smem + OFF_RED);
-    float* m_used = reinterpret_cast<float*>(smem + OFF_MUSED);
+    float* m_neg = reinterpret_cast<float*>(smem + OFF_MNEG);
     float* alpha_s = reinterpret_cast<float*>(smem + OFF_ALPHA);
     float* invl_s = reinterpret_cast<float*>(smem + OFF_INVL);
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + OFF_BAR);
@@ -536,15 +536,15 @@ __global__ void __maxnreg__(kMaxRegs)   // kThreads threads, one CTA per SM
             if (item < 0) continue;
             const Item I = decode_item(p, item);
             const int32_t* ir = p.idx + (int64_t)I.row * p.top_k;
-            named_bar_sync(1, kWorkers);  // previous item's readers of m_used / invl / item_T are done
-            if (tid < kH) m_used[tid] = -INFINITY;
+            named_bar_sync(1, kWorkers);  // previous item's readers of m_neg / invl / item_T are done
+            if (tid < kH) m_neg[tid] = INFINITY;
             if (ww == 0) {   // one warp finds the item's tile count for all
                 const int tt = item_tiles(p, I, lane);
                 if (lane == 0) *item_T = tt;
             }
-            float l_part[kHG];
+            float2 l2[kHG / 2];   // row sums of heads (h0 + 2i, h0 + 2i + 1)
 #pragma unroll
-            for (int h = 0; h < kHG; ++h) l_part[h] = 0.f;
+            for (int i = 0; i < kHG / 2; ++i) l2[i] = make_float2(0.f, 0.f);
             named_bar_sync(1, kWorkers);
             const int T = *item_T;
             for (int t = 0; t < T; ++t, ++gt) {
@@ -552,42 +552,53 @@ __global__ void __maxnreg__(kMaxRegs)   // kThreads threads, one CTA per SM
                 const int j = (slot < I.slot_end) ? __ldg(ir + slot) : -1;  // issued before the wait
                 gok = gok && worker_wait(s_full, gt & 1, abort_flag, p.status);
                 tc_fence_after();
-                float x[kHG];
-                {   // the two issuers' partial sums
+                const bool kvalid = (j >= 0) && (j < I.bound);
+                // This key's scores for heads h0..h0+15 as pairs (packed f32x2 arithmetic): the two
+                // issuers' partial sums added, plus -inf for a padding slot, so that neither the
+                // reference check nor the probability needs the key's validity again.
+                float2 x2[kHG / 2];
+                {
                     uint32_t v[kHG], u[kHG];
                     tmem_ld16(tmem_base + lane_addr + TM_S + h0, v);
                     tmem_ld16(tmem_base + lane_addr + TM_S + 64 + h0, u);
                     tmem_ld_wait();
+                    const float kb = kvalid ? 0.f : -INFINITY;
 #pragma unroll
-                    for (int h = 0; h < kHG; ++h) x[h] = __uint_as_float(v[h]) + __uint_as_float(u[h]);
+                    for (int i = 0; i < kHG / 2; ++i) {
+                        const float2 a = make_float2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]));
+                        const float2 b = make_float2(__uint_as_float(u[2 * i]), __uint_as_float(u[2 * i + 1]));
+                        x2[i] = __fadd2_rn(__fadd2_rn(a, b), make_float2(kb, kb));
+                    }
                 }
                 tc_fence_before();
-                const bool kvalid = (j >= 0) && (j < I.bound);
-                // Reference maxima (scaled, log2 units), one per head: set from the item's
-                // first tile, afterwards moved only when a score exceeds its head's reference
+                // Reference maxima (scaled, log2 units), one per head, kept negated: set from the
+                // item's first tile, afterwards moved only when a score exceeds its head's reference
                 // by more than 2^16 (checked per thread; rare), so the common path has no
-                // cross-thread reduction.  The shifted exponent e = scale*log2(e)*s - m serves
-                // both the check and the probability.  Before the first tile every reference
-                // is -inf, so any valid score counts as exceeding it.  The scale is > 0, so
-                // maxima of the raw scores are maxima of the scaled ones.
-                float mr[kHG];
+                // cross-thread reduction.  The shifted exponent e = scale*log2(e)*s - m serves both
+                // the check and the probability.  Before the first tile every reference is -inf, so
+                // any valid score counts as exceeding it (a padding slot gives -inf or NaN, which
+                // never does).  The scale is > 0, so maxima of the raw scores are maxima of the
+                // scaled ones.
+                const float2 sc2 = make_float2(p.scale_log2, p.scale_log2);
+                float2 e2[kHG / 2];
 #pragma unroll
                 for (int h4 = 0; h4 < kHG / 4; ++h4) {
-                    const float4 m4 = reinterpret_cast<const float4*>(m_used + h0)[h4];
-                    mr[4 * h4 + 0] = m4.x;
-                    mr[4 * h4 + 1] = m4.y;
-                    mr[4 * h4 + 2] = m4.z;
-                    mr[4 * h4 + 3] = m4.w;
+                    const float4 n4 = reinterpret_cast<const float4*>(m_neg + h0)[h4];
+                    e2[2 * h4] = __ffma2_rn(x2[2 * h4], sc2, make_float2(n4.x, n4.y));
+                    e2[2 * h4 + 1] = __ffma2_rn(x2[2 * h4 + 1], sc2, make_float2(n4.z, n4.w));
                 }
                 bool viol = false;
 #pragma unroll
-                for (int h = 0; h < kHG; ++h) viol |= kvalid && (fmaf(x[h], p.scale_log2, -mr[h]) > kRescaleThreshold);
+                for (int i = 0; i < kHG / 2; ++i) viol |= (e2[i].x > kRescaleThreshold) || (e2[i].y > kRescaleThreshold);
                 const bool need_red = named_bar_or(group_bar, kGroupThreads, viol);
                 bool any_upd = false;
                 if (need_red) {
                     float xm[kHG];
 #pragma unroll
-                    for (int h = 0; h < kHG; ++h) xm[h] = kvalid ? x[h] : -INFINITY;
+                    for (int i = 0; i < kHG / 2; ++i) {
+                        xm[2 * i] = x2[i].x;       // -inf for a padding slot
+                        xm[2 * i + 1] = x2[i].y;
+                    }
                     const float r = warp_transpose_reduce16<true>(xm, lane);
                     if ((lane & 1u) == 0) red[quad * kH + h0 + (int)(lane >> 1)] = r;
                     named_bar_sync(group_bar, kGroupThreads);
@@ -595,11 +606,11 @@ __global__ void __maxnreg__(kMaxRegs)   // kThreads threads, one CTA per SM
                     if (ww == 4 * hg && lane < kHG) {   // one lane per head of the group
                         const int h = h0 + (int)lane;
                         const float mt = p.scale_log2 * fmaxf(fmaxf(red[h], red[kH + h]), fmaxf(red[2 * kH + h], red[3 * kH + h]));
-                        const float mo = m_used[h];
+                        const float mo = -m_neg[h];
                         float a = 1.f;
                         if (mt > -INFINITY && (mo == -INFINITY || mt > mo + kRescaleThreshold)) {
                             a = (mo == -INFINITY) ? 0.f : ex2_approx(mo - mt);
-                            m_used[h] = mt;
+                            m_neg[h] = -mt;
                             upd = (mo != -INFINITY);
                         }
                         alpha_s[h] = a;
@@ -607,20 +618,16 @@ __global__ void __maxnreg__(kMaxRegs)   // kThreads threads, one CTA per SM
                     any_upd = named_bar_or(group_bar, kGroupThreads, upd);
 #pragma unroll
                     for (int h4 = 0; h4 < kHG / 4; ++h4) {
-                        const float4 m4 = reinterpret_cast<const float4*>(m_used + h0)[h4];
-                        mr[4 * h4 + 0] = m4.x;
-                        mr[4 * h4 + 1] = m4.y;
-                        mr[4 * h4 + 2] = m4.z;
-                        mr[4 * h4 + 3] = m4.w;
+                        const float4 n4 = reinterpret_cast<const float4*>(m_neg + h0)[h4];
+                        e2[2 * h4] = __ffma2_rn(x2[2 * h4], sc2, make_float2(n4.x, n4.y));
+                        e2[2 * h4 + 1] = __ffma2_rn(x2[2 * h4 + 1], sc2, make_float2(n4.z, n4.w));
                     }
                     if (any_upd) {
 #pragma unroll
                         for (int h4 = 0; h4 < kHG / 4; ++h4) {
                             const float4 a4 = reinterpret_cast<const float4*>(alpha_s + h0)[h4];
-                            l_part[4 * h4 + 0] *= a4.x;
-                            l_part[4 * h4 + 1] *= a4.y;
-                            l_part[4 * h4 + 2] *= a4.z;
-                            l_part[4 * h4 + 3] *= a4.w;
+                            l2[2 * h4] = __fmul2_rn(l2[2 * h4], make_float2(a4.x, a4.y));
+                            l2[2 * h4 + 1] = __fmul2_rn(l2[2 * h4 + 1], make_float2(a4.z, a4.w));
                         }
                     }
                 }
@@ -628,12 +635,10 @@ __global__ void __maxnreg__(kMaxRegs)   // kThreads threads, one CTA per SM
                 // rounded to bf16 for the MMA.
                 uint32_t packed[kHG / 2];
 #pragma unroll
-                for (int h2 = 0; h2 < kHG / 2; ++h2) {
-                    const float p0 = ex2_approx(kvalid ? fmaf(x[2 * h2], p.scale_log2, -mr[2 * h2]) : -INFINITY);
-                    const float p1 = ex2_approx(kvalid ? fmaf(x[2 * h2 + 1], p.scale_log2, -mr[2 * h2 + 1]) : -INFINITY);
-                    packed[h2] = pack_bf16x2(p0, p1);
-                    l_part[2 * h2] += p0;
-                    l_part[2 * h2 + 1] += p1;
+                for (int i = 0; i < kHG / 2; ++i) {
+                    const float2 pr = make_float2(ex2_approx(e2[i].x), ex2_approx(e2[i].y));
+                    packed[i] = pack_bf16x2(pr.x, pr.y);
+                    l2[i] = __fadd2_rn(l2[i], pr);
                 }
                 // P^T row `key`, heads h0..h0+15: 16-byte chunks 2hg and 2hg+1 of the swizzled 128-byte row
 #pragma unroll
@@ -668,6 +673,12 @@ __global__ void __maxnreg__(kMaxRegs)   // kThreads threads, one CTA per SM
             }
             // ---------------- final: l = sum of partial row sums; out = O^T / l
             {
+                float l_part[kHG];
+#pragma unroll
+                for (int i = 0; i < kHG / 2; ++i) {
+                    l_part[2 * i] = l2[i].x;
+                    l_part[2 * i + 1] = l2[i].y;
+                }
                 const float r = warp_transpose_reduce16<false>(l_part, lane);
                 if ((lane & 1u) == 0) red[quad * kH + h0 + (int)(lane >> 1)] = r;
             }
@@ -681,7 +692,7 @@ __global__ void __maxnreg__(kMaxRegs)   // kThreads threads, one CTA per SM
             if (tid < kH) {
                 const float l = red[tid] + red[kH + tid] + red[2 * kH + tid] + red[3 * kH + tid];
                 invl_s[tid] = (l > 0.f) ? 1.f / l : 0.f;
-                lse_h = (l > 0.f) ? (m_used[tid] + log2f(l)) * 0.6931471805599453f : -INFINITY;
+                lse_h = (l > 0.f) ? (log2f(l) - m_neg[tid]) * 0.6931471805599453f : -INFINITY;
             }
             named_bar_sync(1, kWorkers);
 #pragma unroll 1
