@@ -92,6 +92,9 @@ constexpr int kGroupThreads = 4 * 32;              // the four warps sharing a h
 constexpr int kSegs = 4;               // PV releases the stage by 128-dim latent chunk (the rope block with the last)
 static_assert(kWorkerWarps == 16 && kTile == 128, "a worker warp copies four rows of each 64-key half");
 constexpr float kRescaleThreshold = 16.0f;  // log2 units
+// m_neg (minus a head's reference maximum) before the reference is set: finite, so that a padding
+// slot's -inf score still gives a -inf exponent (probability 0) while a valid score exceeds it
+constexpr float kNoRef = 3.0e38f;
 
 // smem layout (1024-aligned base)
 constexpr int OFF_Q = 0;                               // 9 x 8 KB
@@ -537,7 +540,7 @@ __global__ void __maxnreg__(kMaxRegs)   // kThreads threads, one CTA per SM
             const Item I = decode_item(p, item);
             const int32_t* ir = p.idx + (int64_t)I.row * p.top_k;
             named_bar_sync(1, kWorkers);  // previous item's readers of m_neg / invl / item_T are done
-            if (tid < kH) m_neg[tid] = INFINITY;
+            if (tid < kH) m_neg[tid] = kNoRef;
             if (ww == 0) {   // one warp finds the item's tile count for all
                 const int tt = item_tiles(p, I, lane);
                 if (lane == 0) *item_T = tt;
@@ -575,9 +578,9 @@ __global__ void __maxnreg__(kMaxRegs)   // kThreads threads, one CTA per SM
                 // item's first tile, afterwards moved only when a score exceeds its head's reference
                 // by more than 2^16 (checked per thread; rare), so the common path has no
                 // cross-thread reduction.  The shifted exponent e = scale*log2(e)*s - m serves both
-                // the check and the probability.  Before the first tile every reference is -inf, so
-                // any valid score counts as exceeding it (a padding slot gives -inf or NaN, which
-                // never does).  The scale is > 0, so maxima of the raw scores are maxima of the
+                // the check and the probability.  Before the first tile no reference is set (m_neg =
+                // kNoRef), so any valid score counts as exceeding it, and a padding slot gives -inf,
+                // which never does.  The scale is > 0, so maxima of the raw scores are maxima of the
                 // scaled ones.
                 const float2 sc2 = make_float2(p.scale_log2, p.scale_log2);
                 float2 e2[kHG / 2];
@@ -606,12 +609,13 @@ __global__ void __maxnreg__(kMaxRegs)   // kThreads threads, one CTA per SM
                     if (ww == 4 * hg && lane < kHG) {   // one lane per head of the group
                         const int h = h0 + (int)lane;
                         const float mt = p.scale_log2 * fmaxf(fmaxf(red[h], red[kH + h]), fmaxf(red[2 * kH + h], red[3 * kH + h]));
+                        const bool unset = (m_neg[h] == kNoRef);
                         const float mo = -m_neg[h];
                         float a = 1.f;
-                        if (mt > -INFINITY && (mo == -INFINITY || mt > mo + kRescaleThreshold)) {
-                            a = (mo == -INFINITY) ? 0.f : ex2_approx(mo - mt);
+                        if (mt > -INFINITY && (unset || mt > mo + kRescaleThreshold)) {
+                            a = unset ? 0.f : ex2_approx(mo - mt);
                             m_neg[h] = -mt;
-                            upd = (mo != -INFINITY);
+                            upd = !unset;
                         }
                         alpha_s[h] = a;
                     }

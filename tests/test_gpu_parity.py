@@ -351,6 +351,10 @@ def test_attention_generator_indices_with_gaps(dsa, oracle_mod):
         pos = np.sort(rng.choice(wl.top_k, size=n, replace=False))
         idx[r, pos] = sel
     idx[3] = -1                        # a row with nothing selected
+    # rows whose first 128-key tile (or first two) is all padding, with keys selected after it
+    for r, start in ((7, 128), (11, 256), (13, 130)):
+        idx[r] = -1
+        idx[r, start:start + 9] = rng.choice(wl.N, size=9, replace=False)
     out, lse = dsa.mla_sparse_attn_prefill(dev(q[0]), dev(kv[0]), dev(idx), W.SCALE, want_lse=True)
     torch.cuda.synchronize()
     o_ref, l_ref = oracle_mod.attention(q[0], kv, idx, np.zeros(wl.L, np.int32), W.SCALE)
